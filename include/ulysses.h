@@ -1,0 +1,189 @@
+/*
+ * ulysses.h -- C ABI of the GB300 (sm_103a) Ulysses sequence-parallel hot path.
+ *
+ * The path (Transformers docs "Ulysses sequence parallelism", introduction and
+ * its all-to-all diagram; Hugging Face Ulysses blog summary, "How Ulysses
+ * Sequence Parallelism Works", steps 3-5):
+ *   1. seq->head all-to-all: P sequence shards [N/P, H, d] become P head
+ *      shards [N, H/P, d];
+ *   2. local attention over every head shard, full sequence, causal, with
+ *      GQA K/V sharing and optional packed-document masking; and its
+ *      backward;
+ *   3. head->seq all-to-all back.
+ * On one GPU the P ranks are P virtual ranks: P contiguous shards inside one
+ * device allocation, so the all-to-all is a device-local permutation.
+ *
+ * Conventions for every call:
+ *  - Pointers named x_*, q, k, v, o, lse, dout, dq, dk, dv and workspace are
+ *    DEVICE pointers owned by the caller; the library never allocates, frees
+ *    or keeps them.  Host pointers are marked _host.
+ *  - Every pointer must be 16-byte aligned (ULY_ERR_MISALIGNED otherwise).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ *    stream) and never synchronise, except ulysses_get_device_status.
+ *  - Arguments are validated on the host before anything is launched; on
+ *    failure nothing is launched and the status says why.
+ *  - dtype: ULY_BF16 (bf16 storage, fp32 accumulation) or ULY_FP32 (fp32
+ *    throughout, the correctness path).
+ *  - Layouts are row-major, outermost first:
+ *      seq layout  : [P][B][N/P][H][d]   (P contiguous sequence shards)
+ *      head layout : [P][B][N][H/P][d]   (P contiguous head shards)
+ *      lse         : [S][B][Hq][N] fp32, natural logarithm of the row's sum
+ *                    of exp(scaled scores)
+ *    where S is the number of head shards an attention call covers.
+ *  - Thread safety: calls on different streams with different buffers and
+ *    workspaces may run concurrently.  The device status word is shared by
+ *    all calls on a device.
+ */
+#ifndef ULYSSES_H
+#define ULYSSES_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ULY_OK = 0,
+    ULY_ERR_INVALID_ARG = 1, /* a size, count or flag is out of range */
+    ULY_ERR_UNSUPPORTED = 2, /* valid for the method, not handled by this build */
+    ULY_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+    ULY_ERR_OVERLAP = 4,     /* input and output buffers overlap */
+    ULY_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
+    ULY_ERR_TIMEOUT = 6,     /* a device-side bounded wait ran out */
+    ULY_ERR_WORKSPACE = 7    /* workspace missing or smaller than required */
+} uly_status;
+
+typedef enum { ULY_BF16 = 0, ULY_FP32 = 1 } uly_dtype;
+
+/* ---------------------------------------------------------------- swaps */
+
+/*
+ * seq->head all-to-all, emulated over P virtual ranks in one allocation.
+ * Source: Transformers docs "Ulysses sequence parallelism", the all-to-all
+ * diagram (rank r keeps every token and receives the contiguous head block
+ * r); blog summary "How Ulysses Sequence Parallelism Works", step 3.
+ *
+ *   x_head[r][b][n][h][k] = x_seq[n / (N/P)][b][n % (N/P)][r*H/P + h][k]
+ *
+ * x_seq  : device, [P][B][N/P][H][d], read only.
+ * x_head : device, [P][B][N][H/P][d], fully written.
+ * B >= 1, N >= 1 with N % P == 0 (sequences are padded to a multiple of the
+ * SP size), H % P == 0 (the number of heads must be divisible by the SP size),
+ * 1 <= P <= H, d in {64, 128}.  The two buffers must not overlap.
+ * The copy is exact (bit for bit) for either dtype.
+ */
+uly_status ulysses_seq_to_head(const void *x_seq, void *x_head, int64_t B, int64_t N, int32_t H,
+                               int32_t d, int32_t P, uly_dtype dtype, void *stream);
+
+/*
+ * head->seq all-to-all: the exact inverse of ulysses_seq_to_head (the second
+ * all-to-all of the same diagram; blog summary step 5).  It is also the
+ * backward of seq->head, and seq->head is the backward of head->seq.
+ *
+ *   x_seq[s][b][t][r*H/P + h][k] = x_head[r][b][s*(N/P) + t][h][k]
+ *
+ * Same argument rules as ulysses_seq_to_head.
+ */
+uly_status ulysses_head_to_seq(const void *x_head, void *x_seq, int64_t B, int64_t N, int32_t H,
+                               int32_t d, int32_t P, uly_dtype dtype, void *stream);
+
+/* ------------------------------------------------------------ attention */
+
+/*
+ * Bytes of device workspace ulysses_attn_fwd (for_bwd = 0) or
+ * ulysses_attn_bwd (for_bwd = 1) needs for these sizes.  Returns 0 for sizes
+ * the call would reject.  num_docs = 0 means one document (no packing).
+ */
+size_t ulysses_attn_workspace_size(int64_t B, int64_t N, int32_t Hq_local, int32_t Hkv_local,
+                                   int32_t d, int32_t num_shards, int32_t num_docs,
+                                   int32_t for_bwd, uly_dtype dtype);
+
+/*
+ * Attention forward over `num_shards` consecutive head shards (blog summary,
+ * step 4 "Local Attention": every rank attends over all N tokens for its
+ * heads).  For shard s, batch b, local query head h (local KV head h / G,
+ * G = Hq_local / Hkv_local), row i:
+ *   s_ij  = softmax_scale * <q_i, k_j>            for allowed j
+ *   lse_i = ln sum_j exp(s_ij)
+ *   o_i   = sum_j exp(s_ij - lse_i) v_j
+ * allowed: j <= i if causal; and doc(i) == doc(j) if cu_seqlens_host is not
+ * NULL (packed documents, the block-diagonal mask of FlashAttention-style
+ * varlen attention that the Transformers docs recommend for packing).
+ *
+ * q, o       : device, [num_shards][B][N][Hq_local][d]
+ * k, v       : device, [num_shards][B][N][Hkv_local][d]
+ * lse        : device fp32, [num_shards][B][Hq_local][N]
+ * cu_seqlens_host : host int32 [num_docs + 1], 0 = cu[0] <= cu[1] <= ... <=
+ *              cu[num_docs] = N, or NULL (one document).  Copied before return.
+ * softmax_scale <= 0 selects 1/sqrt(d).
+ * workspace  : device, >= ulysses_attn_workspace_size(..., for_bwd=0) bytes.
+ * Requires Hq_local % Hkv_local == 0, d in {64, 128} (bf16: d == 128).
+ */
+uly_status ulysses_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int64_t B, int64_t N, int32_t Hq_local, int32_t Hkv_local, int32_t d,
+                            int32_t num_shards, int32_t causal, const int32_t *cu_seqlens_host,
+                            int32_t num_docs, float softmax_scale, uly_dtype dtype, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
+ * Attention backward (the gradient of ulysses_attn_fwd, which training needs;
+ * the Trainer discussion in the blog summary requires the gradients to be
+ * correct).  With P_ij = exp(s_ij - lse_i) and D_i = <dO_i, O_i>:
+ *   dV_j = sum_i P_ij dO_i
+ *   dS_ij = P_ij (<dO_i, v_j> - D_i)
+ *   dQ_i = softmax_scale sum_j dS_ij k_j
+ *   dK_j = softmax_scale sum_i dS_ij q_i
+ * dK and dV are summed over the G query heads sharing a KV head.
+ *
+ * q, k, v, o, lse : as returned/used by ulysses_attn_fwd (o and lse from it).
+ * dout, dq        : device, like q.   dk, dv : device, like k.  All written.
+ * workspace       : device, >= ulysses_attn_workspace_size(..., for_bwd=1);
+ *                   holds fp32 scratch (D, scaled lse, the dQ accumulator).
+ * Other arguments as in ulysses_attn_fwd.
+ */
+uly_status ulysses_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                            const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                            int64_t B, int64_t N, int32_t Hq_local, int32_t Hkv_local, int32_t d,
+                            int32_t num_shards, int32_t causal, const int32_t *cu_seqlens_host,
+                            int32_t num_docs, float softmax_scale, uly_dtype dtype, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------ diagnostics */
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  ULY_OK if no kernel reported a problem since the last read;
+ * ULY_ERR_TIMEOUT if a bounded device-side wait ran out (the kernel then
+ * stopped early and its outputs are invalid); ULY_ERR_INVALID_ARG if a kernel
+ * rejected its launch configuration; ULY_ERR_CUDA on a CUDA error.
+ * If site_out is not NULL it receives the id of the first wait that ran out.
+ */
+uly_status ulysses_get_device_status(void *stream, uint32_t *site_out);
+
+/*
+ * Sets the per-wait limit (nanoseconds, >= 1000) of every bounded device
+ * wait launched afterwards by this process.  Default: 2 s.
+ */
+uly_status ulysses_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Launches one tiny kernel whose mbarrier wait can never complete (nothing
+ * arrives on it), with a limit of limit_ns.  The wait gives up, records
+ * ULY_ERR_TIMEOUT in the device status word and the kernel returns.  Used by
+ * tests of the timeout path; it faults nothing and hangs nothing.
+ */
+uly_status ulysses_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *ulysses_status_string(uly_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t ulysses_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ULYSSES_H */

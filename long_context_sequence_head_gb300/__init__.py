@@ -1,0 +1,217 @@
+"""Python binding of the GB300 Ulysses library (``include/ulysses.h``).
+
+Argument marshalling only: every step of the path (the seq<->head swaps, the
+attention forward and backward) runs in the CUDA kernels of
+``_build/libulysses_gb300.so``.  PyTorch provides device memory and streams.
+There is no CPU fallback: if the library is missing, importing the functions
+raises, and every call checks the status the C ABI returns.
+
+The functions keep the C names.  Tensors must be contiguous CUDA tensors in
+the layouts of the header:
+    seq layout  [P][B][N/P][H][d]     head layout [P][B][N][H/P][d]
+    q, o, dout  [S][B][N][Hq][d]      k, v        [S][B][N][Hkv][d]
+    lse         [S][B][Hq][N] fp32
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import build as _build_mod
+
+ULY_OK = 0
+ULY_BF16 = 0
+ULY_FP32 = 1
+_STATUS = {0: "ULY_OK", 1: "ULY_ERR_INVALID_ARG", 2: "ULY_ERR_UNSUPPORTED", 3: "ULY_ERR_MISALIGNED",
+           4: "ULY_ERR_OVERLAP", 5: "ULY_ERR_CUDA", 6: "ULY_ERR_TIMEOUT", 7: "ULY_ERR_WORKSPACE"}
+
+# every symbol include/ulysses.h declares
+EXPORTED = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_workspace_size",
+            "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_get_device_status",
+            "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout",
+            "ulysses_status_string", "ulysses_version")
+
+
+class UlyssesError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {_STATUS.get(status, status)}")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build_mod.SO_PATH
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load the shared library (it must have been built by ``build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"CUDA library not built: {path} is missing; run "
+                               "`python -m long_context_sequence_head_gb300.build`")
+        _build_mod.build()
+    lib = ctypes.CDLL(path)
+    i64, i32, u64, vp, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_float
+    sz = ctypes.c_size_t
+    lib.ulysses_seq_to_head.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, vp]
+    lib.ulysses_head_to_seq.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, vp]
+    lib.ulysses_attn_workspace_size.argtypes = [i64, i64, i32, i32, i32, i32, i32, i32, i32]
+    lib.ulysses_attn_workspace_size.restype = sz
+    lib.ulysses_attn_fwd.argtypes = [vp] * 5 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp, sz, vp]
+    lib.ulysses_attn_bwd.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp, sz, vp]
+    lib.ulysses_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.ulysses_set_wait_limit_ns.argtypes = [u64]
+    lib.ulysses_selftest_wait_timeout.argtypes = [u64, vp]
+    lib.ulysses_status_string.argtypes = [i32]
+    lib.ulysses_status_string.restype = ctypes.c_char_p
+    lib.ulysses_version.restype = i32
+    for name in ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_fwd", "ulysses_attn_bwd",
+                 "ulysses_get_device_status", "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout"):
+        getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, st: int):
+    if st != ULY_OK:
+        raise UlyssesError(fn, st)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return ULY_BF16
+    if t.dtype == torch.float32:
+        return ULY_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _dev(*ts: torch.Tensor):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _cu(cu_seqlens):
+    if cu_seqlens is None:
+        return None, 0, None
+    arr = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    return arr.ctypes.data_as(ctypes.c_void_p), len(arr) - 1, arr
+
+
+# ------------------------------------------------------------------ swaps
+
+def ulysses_seq_to_head(x_seq: torch.Tensor, x_head: torch.Tensor, P: int, stream=None) -> torch.Tensor:
+    """[P][B][N/P][H][d] -> [P][B][N][H/P][d] (see include/ulysses.h)."""
+    _dev(x_seq, x_head)
+    Ps, B, Np, H, d = x_seq.shape
+    if Ps != P or tuple(x_head.shape) != (P, B, Np * P, H // P, d) or x_head.dtype != x_seq.dtype:
+        raise ValueError("x_head must be [P][B][N][H/P][d] with the dtype of x_seq")
+    _check("ulysses_seq_to_head", load().ulysses_seq_to_head(
+        x_seq.data_ptr(), x_head.data_ptr(), B, Np * P, H, d, P, _dt(x_seq), _stream(stream)))
+    return x_head
+
+
+def ulysses_head_to_seq(x_head: torch.Tensor, x_seq: torch.Tensor, P: int, stream=None) -> torch.Tensor:
+    """[P][B][N][H/P][d] -> [P][B][N/P][H][d] (see include/ulysses.h)."""
+    _dev(x_head, x_seq)
+    Ps, B, N, Hp, d = x_head.shape
+    if Ps != P or tuple(x_seq.shape) != (P, B, N // P, Hp * P, d) or x_seq.dtype != x_head.dtype:
+        raise ValueError("x_seq must be [P][B][N/P][H][d] with the dtype of x_head")
+    _check("ulysses_head_to_seq", load().ulysses_head_to_seq(
+        x_head.data_ptr(), x_seq.data_ptr(), B, N, Hp * P, d, P, _dt(x_head), _stream(stream)))
+    return x_seq
+
+
+# -------------------------------------------------------------- attention
+
+def ulysses_attn_workspace_size(B: int, N: int, Hq_local: int, Hkv_local: int, d: int, num_shards: int,
+                                num_docs: int, for_bwd: bool, dtype: torch.dtype) -> int:
+    dt = ULY_BF16 if dtype == torch.bfloat16 else ULY_FP32
+    return int(load().ulysses_attn_workspace_size(B, N, Hq_local, Hkv_local, d, num_shards, num_docs,
+                                                  int(bool(for_bwd)), dt))
+
+
+def _workspace(workspace, nbytes: int, device) -> torch.Tensor:
+    if workspace is None:
+        return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace too small: need {nbytes} bytes")
+    return workspace
+
+
+def ulysses_attn_fwd(q, k, v, o, lse, causal: bool = True, cu_seqlens: Optional[Sequence[int]] = None,
+                     softmax_scale: float = 0.0, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Attention forward over head shards; writes o and lse (see include/ulysses.h)."""
+    _dev(q, k, v, o, lse)
+    S, B, N, Hq, d = q.shape
+    Hkv = k.shape[3]
+    cu_p, nd, _keep = _cu(cu_seqlens)
+    need = ulysses_attn_workspace_size(B, N, Hq, Hkv, d, S, nd, False, q.dtype)
+    ws = _workspace(workspace, need, q.device)
+    _check("ulysses_attn_fwd", load().ulysses_attn_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, N, Hq, Hkv, d, S,
+        int(bool(causal)), cu_p, nd, float(softmax_scale), _dt(q), ws.data_ptr(),
+        ws.numel() * ws.element_size(), _stream(stream)))
+    return o, lse
+
+
+def ulysses_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = True,
+                     cu_seqlens: Optional[Sequence[int]] = None, softmax_scale: float = 0.0,
+                     workspace: Optional[torch.Tensor] = None, stream=None):
+    """Attention backward; writes dq, dk, dv (see include/ulysses.h)."""
+    _dev(q, k, v, o, lse, dout, dq, dk, dv)
+    S, B, N, Hq, d = q.shape
+    Hkv = k.shape[3]
+    cu_p, nd, _keep = _cu(cu_seqlens)
+    need = ulysses_attn_workspace_size(B, N, Hq, Hkv, d, S, nd, True, q.dtype)
+    ws = _workspace(workspace, need, q.device)
+    _check("ulysses_attn_bwd", load().ulysses_attn_bwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, N, Hq, Hkv, d, S, int(bool(causal)), cu_p, nd,
+        float(softmax_scale), _dt(q), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
+    return dq, dk, dv
+
+
+# ------------------------------------------------------------ diagnostics
+
+def ulysses_get_device_status(stream=None):
+    """Synchronise the stream, read and clear the device status.  Returns (status, site)."""
+    site = ctypes.c_uint32(0)
+    st = load().ulysses_get_device_status(_stream(stream), ctypes.byref(site))
+    return int(st), int(site.value)
+
+
+def ulysses_set_wait_limit_ns(limit_ns: int) -> None:
+    _check("ulysses_set_wait_limit_ns", load().ulysses_set_wait_limit_ns(int(limit_ns)))
+
+
+def ulysses_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check("ulysses_selftest_wait_timeout", load().ulysses_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def ulysses_status_string(status: int) -> str:
+    return load().ulysses_status_string(int(status)).decode()
+
+
+def ulysses_version() -> int:
+    return int(load().ulysses_version())

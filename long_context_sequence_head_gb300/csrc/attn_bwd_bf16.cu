@@ -1,0 +1,602 @@
+// Attention backward for the bf16 path on tcgen05 tensor cores, head_dim 128.
+//
+// Gradient of the forward in attn_fwd_bf16.cu (training needs it; the blog
+// summary's Trainer discussion requires correct gradients).  With
+// P_ij = exp(s_ij - lse_i) recomputed from the stored log-sum-exp and
+// D_i = <dO_i, O_i>:
+//   dV_j = sum_i P_ij dO_i,   dS_ij = P_ij (<dO_i, v_j> - D_i),
+//   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i,
+// dK, dV summed over the G query heads that share KV head j.
+//
+// Kernels:
+//   bwd_pre    : D_i and lse_i*log2(e) into fp32 scratch (padded rows get
+//                D = 0, lse = +inf so their probabilities are exactly 0).
+//   bwd_main   : one CTA per (shard*batch, KV head, 128-key tile).  K and V
+//                stay in shared memory; the CTA walks the G query heads of
+//                the group and every 128-row query tile that may attend to
+//                its keys.  dK and dV accumulate in TMEM across the whole
+//                group (no atomics); each dQ partial is added into an fp32
+//                accumulator with coalesced vector reductions.
+//   dq_convert : fp32 accumulator * scale -> bf16 dQ in the head layout.
+//
+// bwd_main warp roles (320 threads):
+//   warps 0-3 : thread = key row j (TMEM lane).  S^T row -> P^T (bf16, into
+//               TMEM for the dV product), dP^T row -> dS^T (bf16, into
+//               shared memory for the dK and dQ products); final dK/dV
+//               epilogue.
+//   warps 4-7 : thread = query row of the current tile; reads the dQ partial
+//               out of TMEM and reduces it into global memory.
+//   warp  8   : TMA producer (K, V once; Q, dO, lse, D per iteration, 2 stages)
+//   warp  9   : tcgen05.mma issuer and TMEM owner.
+// TMEM (512 columns): S^T/P^T | dP^T, later dQ | dV | dK.
+// Per (key tile, query tile) the MMAs are S^T = K Q^T, dP^T = V dO^T,
+// dV += P^T dO, dK += dS^T Q, dQ = dS K.
+#include "uly_internal.h"
+
+namespace uly {
+namespace {
+
+constexpr int kBM = 128;  // query rows per tile
+constexpr int kBN = 128;  // keys per tile
+constexpr int kD = 128;
+constexpr int kTile = kBM * kD * 2;  // 32 KB
+constexpr int kChunk = 128 * 64 * 2; // 16 KB
+constexpr int kThreads = 320;
+
+struct BwdSmem {
+    static constexpr int kK = 0;
+    static constexpr int kV = kTile;
+    static constexpr int kQ = 2 * kTile;       // [2]
+    static constexpr int kdO = 4 * kTile;      // [2]
+    static constexpr int kdS = 6 * kTile;
+    static constexpr int kLse = 7 * kTile;     // [2][128] fp32
+    static constexpr int kDv = kLse + 1024;    // [2][128] fp32
+    static constexpr int kBars = kDv + 1024;
+    static constexpr int kTotal = kBars + 128;
+};
+
+struct BwdParams {
+    int64_t SB, N, Npad;
+    int Hq, Hkv, G, n_ktiles;
+    int causal;
+    const int32_t *cu;
+    int num_docs;
+    float scale_log2;
+    float scale;
+    const float *lse2;  // [SB][Hq][Npad]
+    const float *Dv;    // [SB][Hq][Npad]
+    float *dq_acc;      // [SB][Hq][Npad/128][32][128][4]
+    uint16_t *dk, *dv;  // [SB][N][Hkv][128]
+    WaitCfg w;
+};
+
+__device__ __forceinline__ void doc_range(const BwdParams &p, int64_t i, int64_t &lo, int64_t &hi)
+{
+    lo = 0;
+    hi = p.N;
+    if (p.cu == nullptr)
+        return;
+    int a = 0, b = p.num_docs;
+    while (b - a > 1) {
+        const int m = (a + b) >> 1;
+        if (static_cast<int64_t>(p.cu[m]) <= i)
+            a = m;
+        else
+            b = m;
+    }
+    lo = p.cu[a];
+    hi = p.cu[a + 1];
+}
+
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// ------------------------------------------------------------------ pre
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *__restrict__ o,
+                                                      const uint16_t *__restrict__ dout,
+                                                      const float *__restrict__ lse, float *__restrict__ lse2,
+                                                      float *__restrict__ Dv, int64_t SB, int64_t N, int64_t Npad,
+                                                      int Hq)
+{
+    // one warp per (sb, h, row); lane reads 4 bf16 of O and dO (8 bytes each)
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t total = SB * Hq * Npad;
+    if (gw >= total)
+        return;
+    const int64_t i = gw % Npad;
+    const int64_t sbh = gw / Npad;
+    const int h = static_cast<int>(sbh % Hq);
+    const int64_t sb = sbh / Hq;
+    if (i >= N) {
+        if (lane == 0) {
+            Dv[gw] = 0.f;
+            lse2[gw] = INFINITY;
+        }
+        return;
+    }
+    const int64_t off = ((sb * N + i) * Hq + h) * kD + lane * 4;
+    const uint2 a = *reinterpret_cast<const uint2 *>(o + off);
+    const uint2 b = *reinterpret_cast<const uint2 *>(dout + off);
+    float acc = bf16lo(a.x) * bf16lo(b.x);
+    acc = fmaf(bf16hi(a.x), bf16hi(b.x), acc);
+    acc = fmaf(bf16lo(a.y), bf16lo(b.y), acc);
+    acc = fmaf(bf16hi(a.y), bf16hi(b.y), acc);
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) {
+        Dv[gw] = acc;
+        lse2[gw] = lse[sbh * N + i] * 1.4426950408889634f;
+    }
+}
+
+// ---------------------------------------------------------- dq convert
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc, uint16_t *__restrict__ dq,
+                                                         int64_t SB, int64_t N, int64_t Npad, int Hq, float scale)
+{
+    // thread -> (sb, h, row, group of 4 columns); lanes vary the group so the
+    // bf16 row writes are contiguous
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t total = SB * Hq * N * 32;
+    if (t >= total)
+        return;
+    const int g = static_cast<int>(t & 31);
+    int64_t rest = t >> 5;
+    const int64_t i = rest % N;
+    rest /= N;
+    const int h = static_cast<int>(rest % Hq);
+    const int64_t sb = rest / Hq;
+    const float4 v = *reinterpret_cast<const float4 *>(
+        acc + (((sb * Hq + h) * (Npad / kBM) + i / kBM) * 32 + g) * (kBM * 4) + (i % kBM) * 4);
+    uint2 out;
+    out.x = pack_bf16x2(v.x * scale, v.y * scale);
+    out.y = pack_bf16x2(v.z * scale, v.w * scale);
+    *reinterpret_cast<uint2 *>(dq + ((sb * N + i) * Hq + h) * kD + g * 4) = out;
+}
+
+// ----------------------------------------------------------------- main
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                         BwdParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    // the shared-memory budget leaves no room to align by hand: the dynamic
+    // window starts 1024-aligned when the kernel declares no static shared
+    // memory; refuse to run otherwise
+    if ((smem_u32(smem_raw) & 1023u) != 0) {
+        if (threadIdx.x == 0)
+            atomicOr(p.w.status, kDevBadArg);
+        return;
+    }
+    uint8_t *smem = smem_raw;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + BwdSmem::kBars);
+    uint64_t *kv_full = bars + 0;
+    uint64_t *q_full = bars + 1;   // [2]
+    uint64_t *q_empty = bars + 3;  // [2]
+    uint64_t *s_full = bars + 5;
+    uint64_t *dp_full = bars + 6;
+    uint64_t *ds_full = bars + 7;
+    uint64_t *ds_empty = bars + 8;
+    uint64_t *dq_full = bars + 9;
+    uint64_t *dq_empty = bars + 10;
+    uint64_t *dkv_done = bars + 11;
+    uint64_t *drain = bars + 12;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = warp_id();
+    const int lane = lane_id();
+
+    // ---- work unit: key tiles with the most query tiles first ----
+    const int64_t per_n = p.SB * p.Hkv;
+    const int n_blk = static_cast<int>(blockIdx.x / per_n);
+    const int kvh = static_cast<int>(blockIdx.x % p.Hkv);
+    const int sb = static_cast<int>((blockIdx.x / p.Hkv) % p.SB);
+    const int64_t kv0 = static_cast<int64_t>(n_blk) * kBN;
+    const int64_t key_last = (kv0 + kBN - 1 < p.N - 1) ? kv0 + kBN - 1 : p.N - 1;
+    int64_t row_lo, row_hi, tmp;
+    doc_range(p, kv0, row_lo, tmp);
+    doc_range(p, key_last, tmp, row_hi);
+    if (p.causal)
+        row_lo = kv0;
+    const int m_lo = static_cast<int>(row_lo / kBM);
+    const int n_m = static_cast<int>((row_hi - 1) / kBM) - m_lo + 1;
+    const int n_it = p.G * n_m;
+
+    if (warp == 8 && lane == 0) {
+        for (int i = 0; i < 13; ++i)
+            mbar_init(&bars[i], 1);
+        mbar_init(ds_full, kBN);
+        mbar_init(dq_empty, kBM);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    const uint32_t tS = tbase, tdP = tbase + 128, tdV = tbase + 256, tdK = tbase + 384;
+
+    if (warp == 8) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            mbar_expect_tx(kv_full, 2 * kTile);
+            tma_load_4d(smem + BwdSmem::kK, &tm_k, kv_full, 0, kvh, static_cast<int>(kv0), sb);
+            tma_load_4d(smem + BwdSmem::kK + kChunk, &tm_k, kv_full, 64, kvh, static_cast<int>(kv0), sb);
+            tma_load_4d(smem + BwdSmem::kV, &tm_v, kv_full, 0, kvh, static_cast<int>(kv0), sb);
+            tma_load_4d(smem + BwdSmem::kV + kChunk, &tm_v, kv_full, 64, kvh, static_cast<int>(kv0), sb);
+            int issued = 0;
+            for (int it = 0; it < n_it && !*abort_flag; ++it) {
+                const int slot = it & 1;
+                const int h = kvh * p.G + it / n_m;
+                const int m = m_lo + it % n_m;
+                if (!mbar_wait(&q_empty[slot], ((it >> 1) & 1) ^ 1, p.w, 0x51)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_expect_tx(&q_full[slot], 2 * kTile + 2 * 512);
+                uint8_t *sq = smem + BwdSmem::kQ + slot * kTile;
+                uint8_t *sdo = smem + BwdSmem::kdO + slot * kTile;
+                tma_load_4d(sq, &tm_q, &q_full[slot], 0, h, m * kBM, sb);
+                tma_load_4d(sq + kChunk, &tm_q, &q_full[slot], 64, h, m * kBM, sb);
+                tma_load_4d(sdo, &tm_do, &q_full[slot], 0, h, m * kBM, sb);
+                tma_load_4d(sdo + kChunk, &tm_do, &q_full[slot], 64, h, m * kBM, sb);
+                const int64_t roff = (static_cast<int64_t>(sb) * p.Hq + h) * p.Npad + static_cast<int64_t>(m) * kBM;
+                bulk_g2s(smem + BwdSmem::kLse + slot * 512, p.lse2 + roff, 512, &q_full[slot]);
+                bulk_g2s(smem + BwdSmem::kDv + slot * 512, p.Dv + roff, 512, &q_full[slot]);
+                ++issued;
+            }
+            if (*abort_flag) {
+                mbar_wait(kv_full, 0, p.w, 0x5f);
+                for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it)
+                    mbar_wait(&q_full[it & 1], (it >> 1) & 1, p.w, 0x5f);
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_kk = idesc_bf16(128, 128, false, false);  // both K-major
+            const uint32_t id_kmn = idesc_bf16(128, 128, false, true);  // B MN-major
+            const uint32_t id_mnmn = idesc_bf16(128, 128, true, true);  // A and B MN-major
+            const uint32_t sK = smem_u32(smem + BwdSmem::kK), sV = smem_u32(smem + BwdSmem::kV);
+            const uint32_t sdS = smem_u32(smem + BwdSmem::kdS);
+            bool ok = mbar_wait(kv_full, 0, p.w, 0x61);
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int slot = it & 1;
+                const uint32_t sQ = smem_u32(smem + BwdSmem::kQ + slot * kTile);
+                const uint32_t sdO = smem_u32(smem + BwdSmem::kdO + slot * kTile);
+                if (!mbar_wait(&q_full[slot], (it >> 1) & 1, p.w, 0x62)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // S^T = K Q^T
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+                    mma_ss(tS, desc_sw128(sK + off, 16, 1024), desc_sw128(sQ + off, 16, 1024), id_kk, kk > 0);
+                }
+                mma_commit(s_full);
+                if (it > 0 && !mbar_wait(dq_empty, (it - 1) & 1, p.w, 0x63)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // dP^T = V dO^T
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+                    mma_ss(tdP, desc_sw128(sV + off, 16, 1024), desc_sw128(sdO + off, 16, 1024), id_kk, kk > 0);
+                }
+                mma_commit(dp_full);
+                if (!mbar_wait(ds_full, it & 1, p.w, 0x64)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // dV += P^T dO   (A = P^T in TMEM, B = dO, d contiguous)
+#pragma unroll
+                for (int kk = 0; kk < kBM / 16; ++kk)
+                    mma_ts(tdV, tS + kk * 8, desc_sw128(sdO + kk * 2048, kChunk, 1024), id_kmn,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+                // dK += dS^T Q   (A = dS^T K-major, B = Q, d contiguous)
+#pragma unroll
+                for (int kk = 0; kk < kBM / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+                    mma_ss(tdK, desc_sw128(sdS + off, 16, 1024), desc_sw128(sQ + kk * 2048, kChunk, 1024), id_kmn,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                // dQ = dS K      (A = dS, query index contiguous; B = K, d contiguous)
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_ss(tdP, desc_sw128(sdS + kk * 2048, kChunk, 1024), desc_sw128(sK + kk * 2048, kChunk, 1024),
+                           id_mnmn, kk > 0);
+                mma_commit(dq_full);
+                mma_commit(ds_empty);
+                mma_commit(&q_empty[slot]);
+            }
+            if (!ok)
+                *abort_flag = 1;
+            mma_commit(dkv_done);
+            mma_commit(drain);
+            mbar_wait(drain, 0, p.w, 0x6f);
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------ P^T / dS^T warpgroup
+        const int j = warp * 32 + lane;  // key row in the tile == TMEM lane
+        const int64_t key = kv0 + j;
+        int64_t lo = 0, hi = 0;  // rows that may attend to this key: [lo, hi)
+        if (key < p.N) {
+            doc_range(p, key, lo, hi);
+            if (p.causal)
+                lo = key;
+        }
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const float sl2 = p.scale_log2;
+        uint8_t *ds_row = smem + BwdSmem::kdS + j * 128;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int slot = it & 1;
+            const int64_t q0 = static_cast<int64_t>(m_lo + it % n_m) * kBM;
+            const float *lse_s = reinterpret_cast<const float *>(smem + BwdSmem::kLse + slot * 512);
+            const float *D_s = reinterpret_cast<const float *>(smem + BwdSmem::kDv + slot * 512);
+            if (!mbar_wait_warp(s_full, it & 1, p.w, 0x71)) {
+                ok = false;
+                break;
+            }
+            // lse and D of this query tile were delivered with Q (same barrier)
+            if (!mbar_wait_warp(&q_full[slot], (it >> 1) & 1, p.w, 0x72)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t u[kBM];
+#pragma unroll
+            for (int cb = 0; cb < kBM; cb += 32)
+                tmem_ld32p(tS + lane_off + cb, u + cb);
+            tmem_ld_wait();
+#pragma unroll
+            for (int cb = 0; cb < kBM; cb += 32)
+                tmem_ld_fence32p(u + cb);
+            const bool full = (q0 >= lo) && (q0 + kBM <= hi);
+            uint32_t pk[kBM / 2];
+#pragma unroll
+            for (int c = 0; c < kBM; c += 4) {
+                const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + c);
+                float pv[4];
+                pv[0] = ex2_approx(fmaf(__uint_as_float(u[c + 0]), sl2, -l4.x));
+                pv[1] = ex2_approx(fmaf(__uint_as_float(u[c + 1]), sl2, -l4.y));
+                pv[2] = ex2_approx(fmaf(__uint_as_float(u[c + 2]), sl2, -l4.z));
+                pv[3] = ex2_approx(fmaf(__uint_as_float(u[c + 3]), sl2, -l4.w));
+                if (!full) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int64_t row = q0 + c + e;
+                        if (row < lo || row >= hi)
+                            pv[e] = 0.f;
+                    }
+                }
+                pk[c / 2] = pack_bf16x2(pv[0], pv[1]);
+                pk[c / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+            }
+            tmem_st32p(tS + lane_off, pk);
+            tmem_st32p(tS + lane_off + 32, pk + 32);
+            // dS^T needs the shared buffer the previous iteration's dK/dQ products read
+            if (it > 0 && !mbar_wait_warp(ds_empty, (it - 1) & 1, p.w, 0x73)) {
+                ok = false;
+                break;
+            }
+            if (!mbar_wait_warp(dp_full, it & 1, p.w, 0x74)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int cb = 0; cb < kBM; cb += 32) {
+                uint32_t dp[32];
+                tmem_ld32p(tdP + lane_off + cb, dp);
+                tmem_ld_wait();
+                tmem_ld_fence32p(dp);
+                uint32_t dsp[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(D_s + cb + c);
+                    const uint32_t pa = pk[(cb + c) / 2], pb = pk[(cb + c) / 2 + 1];
+                    const float ds0 = bf16lo(pa) * (__uint_as_float(dp[c + 0]) - d4.x);
+                    const float ds1 = bf16hi(pa) * (__uint_as_float(dp[c + 1]) - d4.y);
+                    const float ds2 = bf16lo(pb) * (__uint_as_float(dp[c + 2]) - d4.z);
+                    const float ds3 = bf16hi(pb) * (__uint_as_float(dp[c + 3]) - d4.w);
+                    dsp[c / 2] = pack_bf16x2(ds0, ds1);
+                    dsp[c / 2 + 1] = pack_bf16x2(ds2, ds3);
+                }
+                // columns cb..cb+31 = four 16-byte units of the swizzled row
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int unit = (cb / 8) + q;  // 0..15
+                    const int chunk = unit >> 3;
+                    const int phys = (unit & 7) ^ (j & 7);
+                    *reinterpret_cast<uint4 *>(ds_row + chunk * kChunk + phys * 16) =
+                        make_uint4(dsp[4 * q], dsp[4 * q + 1], dsp[4 * q + 2], dsp[4 * q + 3]);
+                }
+            }
+            fence_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(ds_full);
+        }
+        if (!ok)
+            *abort_flag = 1;
+        // ---- dK, dV epilogue ----
+        if (mbar_wait_warp(dkv_done, 0, p.w, 0x78) && ok) {
+            tc_fence_after();
+            const bool store = key < p.N;
+            uint16_t *dkp = p.dk + ((static_cast<int64_t>(sb) * p.N + (store ? key : 0)) * p.Hkv + kvh) * kD;
+            uint16_t *dvp = p.dv + ((static_cast<int64_t>(sb) * p.N + (store ? key : 0)) * p.Hkv + kvh) * kD;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t src = which ? tdK : tdV;
+                const float f = which ? p.scale : 1.f;
+                uint16_t *dst = which ? dkp : dvp;
+#pragma unroll
+                for (int cb = 0; cb < kD; cb += 32) {
+                    uint32_t x[32];
+                    tmem_ld32p(src + lane_off + cb, x);  // warp-collective: all lanes
+                    tmem_ld_wait();
+                    tmem_ld_fence32p(x);
+                    uint32_t o16[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        o16[c] = (n_it > 0) ? pack_bf16x2(__uint_as_float(x[2 * c]) * f,
+                                                          __uint_as_float(x[2 * c + 1]) * f)
+                                            : 0u;
+                    if (store) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            reinterpret_cast<uint4 *>(dst + cb)[c] =
+                                make_uint4(o16[4 * c], o16[4 * c + 1], o16[4 * c + 2], o16[4 * c + 3]);
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------ dQ warpgroup
+        const int r = (warp - 4) * 32 + lane;  // query row within the tile
+        const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int h = kvh * p.G + it / n_m;
+            const int m = m_lo + it % n_m;
+            if (!mbar_wait_warp(dq_full, it & 1, p.w, 0x81)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t x[kD];
+#pragma unroll
+            for (int cb = 0; cb < kD; cb += 32)
+                tmem_ld32p(tdP + lane_off + cb, x + cb);
+            tmem_ld_wait();
+#pragma unroll
+            for (int cb = 0; cb < kD; cb += 32)
+                tmem_ld_fence32p(x + cb);
+            tc_fence_before();
+            mbar_arrive(dq_empty);
+            if (static_cast<int64_t>(m) * kBM + r < p.N) {
+                float *base = p.dq_acc + (((static_cast<int64_t>(sb) * p.Hq + h) * (p.Npad / kBM) + m) * 32) *
+                                             (kBM * 4) +
+                              r * 4;
+#pragma unroll
+                for (int g = 0; g < 32; ++g)
+                    red_add_v4(base + g * (kBM * 4), __uint_as_float(x[4 * g]), __uint_as_float(x[4 * g + 1]),
+                               __uint_as_float(x[4 * g + 2]), __uint_as_float(x[4 * g + 3]));
+            }
+        }
+        if (!ok)
+            *abort_flag = 1;
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9)
+        tmem_dealloc(tbase, 512);
+}
+
+CUresult make_map(CUtensorMap *map, const void *base, int64_t SB, int64_t N, int H)
+{
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(SB)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(H) * kD * 2,
+                             static_cast<cuuint64_t>(N) * H * kD * 2};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return tensor_map_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
+                                 const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                                 const BwdScratch &scr, cudaStream_t stream)
+{
+    if (s.d != kD)
+        return cudaErrorInvalidValue;
+    CUtensorMap tq, tk, tv, tdo;
+    if (make_map(&tq, q, s.SB, s.N, s.Hq) != CUDA_SUCCESS || make_map(&tk, k, s.SB, s.N, s.Hkv) != CUDA_SUCCESS ||
+        make_map(&tv, v, s.SB, s.N, s.Hkv) != CUDA_SUCCESS || make_map(&tdo, dout, s.SB, s.N, s.Hq) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const int64_t Npad = scr.Npad;
+    cudaError_t e;
+    // 1. D, lse*log2(e); 2. zero the dQ accumulator
+    {
+        const int64_t warps = s.SB * s.Hq * Npad;
+        const int64_t blocks = (warps * 32 + 255) / 256;
+        bwd_pre_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const uint16_t *>(o), static_cast<const uint16_t *>(dout), lse, scr.lse2, scr.D, s.SB, s.N,
+            Npad, s.Hq);
+        e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+        e = cudaMemsetAsync(scr.dq_acc, 0, static_cast<size_t>(s.SB) * s.Hq * Npad * kD * sizeof(float), stream);
+        if (e != cudaSuccess)
+            return e;
+    }
+    // 3. main kernel
+    BwdParams p;
+    p.SB = s.SB;
+    p.N = s.N;
+    p.Npad = Npad;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.G = s.Hq / s.Hkv;
+    p.n_ktiles = static_cast<int>((s.N + kBN - 1) / kBN);
+    p.causal = s.causal;
+    p.cu = s.cu_dev;
+    p.num_docs = s.num_docs;
+    p.scale_log2 = s.scale * 1.4426950408889634f;
+    p.scale = s.scale;
+    p.lse2 = scr.lse2;
+    p.Dv = scr.D;
+    p.dq_acc = scr.dq_acc;
+    p.dk = static_cast<uint16_t *>(dk);
+    p.dv = static_cast<uint16_t *>(dv);
+    p.w = wait_cfg();
+    const size_t smem = BwdSmem::kTotal;
+    e = cudaFuncSetAttribute(attn_bwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess)
+        return e;
+    const int64_t units = s.SB * s.Hkv * p.n_ktiles;
+    attn_bwd_bf16_kernel<<<static_cast<unsigned>(units), kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    // 4. dQ = scale * accumulator -> bf16
+    {
+        const int64_t total = s.SB * s.Hq * s.N * 32;
+        dq_convert_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
+            scr.dq_acc, static_cast<uint16_t *>(dq), s.SB, s.N, Npad, s.Hq, s.scale);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace uly
