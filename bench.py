@@ -1,0 +1,399 @@
+"""Benchmark of one Ulysses attention layer step on GB300.
+
+A step is the whole hot path over one batch of synthetic input:
+  seq->head swap of Q, K, V  ->  attention forward  ->  head->seq swap of O
+  ->  seq->head swap of dO  ->  attention backward  ->  head->seq swap of dQ, dK, dV
+through the library's C ABI (via its Python binding).
+
+Default workload: Qwen3-4B-shaped attention at long context -- batch 1,
+N = 65536 tokens, P = 4 virtual ranks, 32 query / 8 KV heads, head_dim 128,
+bf16, causal, Q/K/V/dO ~ N(0, 1).
+
+Printed JSON line (rank 0): value = attention fwd+bwd TFLOP/s of the whole
+step, FLOPs counted algorithmically over the allowed (i, j) pairs only
+(forward 4*d*Hq*pairs; backward 2.5x forward, i.e. five products per pair
+including the recomputed scores), divided by the step's device time.
+
+--gpus N under torchrun runs N independent replicas (the method's data path
+is emulated on one GPU; there is no cross-GPU exchange), weak scaling.
+--impl reference times the fp64 CPU oracle on bounded samples of the same
+workload (the reference arm of this benchmark).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal attn fwd+bwd TFLOP/s (% bf16 TC peak) & tokens/s; layout-swap GB/s"
+UNIT = "TFLOP/s"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _pairs(N: int, cu) -> int:
+    if cu is None:
+        return N * (N + 1) // 2
+    import numpy as np
+    L = np.diff(np.asarray(cu, dtype=np.int64))
+    return int((L * (L + 1) // 2).sum())
+
+
+def _workload(name):
+    from ulysses_inputs import WORKLOADS, cu_seqlens_from_lengths, doc_lengths
+    w = WORKLOADS[name]
+    cu = cu_seqlens_from_lengths(doc_lengths(w.N, w.P, seed=3)) if w.packed_docs else None
+    return w, cu
+
+
+def _flops(w, cu):
+    fwd = 4.0 * w.d * (w.Hp * w.shards_timed) * w.B * _pairs(w.N, cu)
+    return fwd, 2.5 * fwd
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[3], parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- our arm
+def run_ours(args, rank, world, dist):
+    import torch
+    import long_context_sequence_head_gb300 as uly
+    from ulysses_inputs import draw_seq_inputs
+
+    uly.load(build_if_missing=True)
+    w, cu = _workload(args.workload)
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    P, S, B, N, d = w.P, w.shards_timed, w.B, w.N, w.d
+    seq = draw_seq_inputs(w, seed=args.seed + rank, device="cuda")
+    q, k, v, do = seq["q"], seq["k"], seq["v"], seq["dout"]
+    bt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    E = lambda *s: torch.empty(*s, dtype=bt, device=dev)
+    qh, kh, vh, doh = E(P, B, N, w.Hp, d), E(P, B, N, w.Hkvp, d), E(P, B, N, w.Hkvp, d), E(P, B, N, w.Hp, d)
+    oh, dqh, dkh, dvh = E(S, B, N, w.Hp, d), E(S, B, N, w.Hp, d), E(S, B, N, w.Hkvp, d), E(S, B, N, w.Hkvp, d)
+    lse = torch.empty(S, B, w.Hp, N, dtype=torch.float32, device=dev)
+    o_seq, dq_seq = E(P, B, N // P, w.Hq, d), E(P, B, N // P, w.Hq, d)
+    dk_seq, dv_seq = E(P, B, N // P, w.Hkv, d), E(P, B, N // P, w.Hkv, d)
+    nd = 0 if cu is None else len(cu) - 1
+    ws_f = torch.empty(uly.ulysses_attn_workspace_size(B, N, w.Hp, w.Hkvp, d, S, nd, False, bt),
+                       dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(uly.ulysses_attn_workspace_size(B, N, w.Hp, w.Hkvp, d, S, nd, True, bt),
+                       dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    full = S == P  # the 1M workload times one head shard; swaps back then need all shards
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        uly.ulysses_seq_to_head(q, qh, P)
+        uly.ulysses_seq_to_head(k, kh, P)
+        uly.ulysses_seq_to_head(v, vh, P)
+        mark(1)
+        uly.ulysses_attn_fwd(qh[:S], kh[:S], vh[:S], oh, lse, causal=w.causal, cu_seqlens=cu, workspace=ws_f)
+        mark(2)
+        if full:
+            uly.ulysses_head_to_seq(oh, o_seq, P)
+        uly.ulysses_seq_to_head(do, doh, P)
+        mark(3)
+        uly.ulysses_attn_bwd(qh[:S], kh[:S], vh[:S], oh, lse, doh[:S], dqh, dkh, dvh, causal=w.causal,
+                             cu_seqlens=cu, workspace=ws_b)
+        mark(4)
+        if full:
+            uly.ulysses_head_to_seq(dqh, dq_seq, P)
+            uly.ulysses_head_to_seq(dkh, dk_seq, P)
+            uly.ulysses_head_to_seq(dvh, dv_seq, P)
+        mark(5)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, site = uly.ulysses_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} at site {site:#x} after warm-up")
+
+    # ---- timed region: device time, inputs resident in HBM
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    st, site = uly.ulysses_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} at site {site:#x} in the timed region")
+    phase = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(args.steps)]
+    ph = [statistics.mean(p[j] for p in phase) for j in range(5)]
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # ---- end to end: host buffers in pinned memory, copies inside the timed region
+    pin = lambda x: torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    h_in = {n: pin(x).copy_(x) for n, x in (("q", q), ("k", k), ("v", v), ("dout", do))}
+    outs = (o_seq, dq_seq, dk_seq, dv_seq) if full else (oh, dqh, dkh, dvh)
+    h_out = [pin(x) for x in outs]
+    h2d = sum(x.numel() * x.element_size() for x in h_in.values())
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    e_steps = max(1, min(args.steps, 5))
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        q.copy_(h_in["q"], non_blocking=True)
+        k.copy_(h_in["k"], non_blocking=True)
+        v.copy_(h_in["v"], non_blocking=True)
+        do.copy_(h_in["dout"], non_blocking=True)
+        step()
+        for hx, dx in zip(h_out, outs):
+            hx.copy_(dx, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    fwd_flops, bwd_flops = _flops(w, cu)
+    step_flops = fwd_flops + bwd_flops
+    ms = elapsed_ms / args.steps
+    value = world * step_flops / (ms * 1e-3) / 1e12
+    hbm, tc_burst, tc_sus, src = _peaks()
+    swap_bytes = 2 * sum(x.numel() * x.element_size() for x in (q, k, v, do))
+    if full:
+        swap_bytes += 2 * sum(x.numel() * x.element_size() for x in (oh, dqh, dkh, dvh))
+    # phases 0, 2 and 4 hold every swap (2 = O back to seq + dO to head)
+    swap_ms = ph[0] + ph[2] + ph[4]
+    bwd_tflops = bwd_flops / (ph[3] * 1e-3) / 1e12
+    fwd_tflops = fwd_flops / (ph[1] * 1e-3) / 1e12
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            tr = json.load(open(tr_path)).get("attn_bwd_bf16_kernel")
+            src_hash = hashlib.sha256(open(os.path.join(
+                ROOT, "long_context_sequence_head_gb300", "csrc", "attn_bwd_bf16.cu"), "rb").read()).hexdigest()
+            if tr and tr.get("src_sha256") == src_hash and tr.get("workload") == args.workload:
+                traffic = tr.get("dram_bytes_per_launch")
+        except Exception:
+            traffic = None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded N(0,1) Q/K/V/dO of the workload's shapes)",
+        "config": {"workload": args.workload, "B": B, "N": N, "P": P, "Hq": w.Hq, "Hkv": w.Hkv, "d": d,
+                   "causal": w.causal, "head_shards_timed": S, "packed_docs": w.packed_docs,
+                   "l2": "no flush: inputs larger than L2 (Q,K,V,dO %.2f GiB per step)" % (
+                       sum(x.numel() * x.element_size() for x in (q, k, v, do)) / 2**30),
+                   "parallelism": f"replicas x{world} (virtual P={P} inside each GPU)"},
+        "tokens_per_s": round(world * B * N / (ms * 1e-3), 1),
+        "attn_fwd_tflops": round(fwd_tflops, 1), "attn_bwd_tflops": round(bwd_tflops, 1),
+        "attn_fwd_bwd_tflops": round(step_flops / ((ph[1] + ph[3]) * 1e-3) / 1e12, 1),
+        "attn_fwd_bwd_frac_of_bf16_peak": round(step_flops / ((ph[1] + ph[3]) * 1e-3) / 1e12 / tc_sus, 3),
+        "flops_no_recompute_tflops": round((fwd_flops * 3.0) / (ms * 1e-3) / 1e12, 2),
+        "swap_gbps": round(swap_bytes / (swap_ms * 1e-3) / 1e9, 1),
+        "swap_frac_of_hbm": round(swap_bytes / (swap_ms * 1e-3) / 1e9 / hbm, 3),
+        "phase_ms": {"swap_qkv": round(ph[0], 3), "attn_fwd": round(ph[1], 3),
+                     "swap_o_and_do": round(ph[2], 3), "attn_bwd": round(ph[3], 3),
+                     "swap_dq_dk_dv": round(ph[4], 3)},
+        "roofline": {"kernel": "ulysses_attn_bwd (bwd_pre + attn_bwd_bf16_kernel + dq_convert)",
+                     "bound": "tensor", "achieved": round(bwd_tflops, 1), "peak": tc_sus, "unit": "TFLOP/s",
+                     "frac": round(bwd_tflops / tc_sus, 3), "traffic": traffic,
+                     "peak_source": f"{src} bf16 sustained (MEASURED_PEAKS.json)" if src == "measured"
+                     else "fallback 1.7 PFLOP/s sustained"},
+        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps * ((8 if full else 4) + 1 + 3),
+    }
+    return line
+
+
+# ------------------------------------------------------------ oracle arm
+def oracle_inputs(w, seed):
+    """The workload's inputs in the oracle's head layout, upcast to fp64 once
+    (outside any timed region)."""
+    import oracle
+    from ulysses_inputs import draw_seq_inputs
+    seq = draw_seq_inputs(w, seed=seed, device="cpu")
+    return {n: oracle._f64(oracle.seq_to_head(seq[n], w.P)[: w.shards_timed]) for n in seq}
+
+
+def oracle_sample(w, cu, heads, rows_per_step, seed):
+    """Time the fp64 oracle on sampled query rows of the workload: forward
+    rows (O, lse) and dQ rows.  Credited FLOPs: 4*d per allowed pair for a
+    forward row (two products), 6*d per allowed pair for a dQ row (scores,
+    dP and dQ products).  Returns (credited_flops, seconds, sample_text)."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    S = w.shards_timed
+    rows = [(int(rng.integers(S)), 0, int(rng.integers(w.Hp)), int(rng.integers(w.N)))
+            for _ in range(rows_per_step)]
+
+    def allowed(i):
+        if cu is None:
+            return i + 1
+        k = int(np.searchsorted(cu, i, side="right")) - 1
+        return i - int(cu[k]) + 1
+    credit = sum(10 * w.d * allowed(i) for *_, i in rows)
+    t0 = time.perf_counter()
+    oracle.attn_fwd_rows(heads["q"], heads["k"], heads["v"], rows, cu_seqlens=cu)
+    oracle.attn_bwd_q_rows(heads["q"], heads["k"], heads["v"], heads["dout"], rows, cu_seqlens=cu)
+    dt = time.perf_counter() - t0
+    return credit, dt, f"{rows_per_step} random query rows (forward + dQ) of {w.name}"
+
+
+def run_reference(args, rank, world):
+    import oracle
+    w, cu = _workload(args.workload)
+    oracle.build()
+    cores = oracle.num_threads()
+    heads = oracle_inputs(w, args.seed)
+    rows = args.oracle_rows
+    for i in range(args.warmup):
+        oracle_sample(w, cu, heads, max(1, rows // 8), args.seed + 1000 + i)
+    tot_c, tot_t = 0.0, 0.0
+    sample = ""
+    for i in range(args.steps):
+        c, t, sample = oracle_sample(w, cu, heads, rows, args.seed + 1 + i)
+        tot_c += c
+        tot_t += t
+    value = tot_c / tot_t / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "N": w.N, "P": w.P, "Hq": w.Hq,
+                                        "Hkv": w.Hkv, "d": w.d},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {sample}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_4b_n65536")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--oracle-rows", type=int, default=384)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, dist)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        w, cu = _workload(args.workload)
+        import oracle
+        oracle.build()
+        heads = oracle_inputs(w, args.seed)
+        c, t, sample = oracle_sample(w, cu, heads, args.oracle_rows, args.seed + 100)
+        line["cpu_baseline"] = {"value": c / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+                                "kind": "oracle", "sample": sample, "seconds": round(t, 2)}
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

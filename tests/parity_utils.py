@@ -20,9 +20,21 @@ def to64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
-def rel_fro(gpu, ref) -> float:
+def rel_fro(gpu, ref, floor: float = 1e-300) -> float:
+    """||gpu - ref||_F / max(||ref||_F, floor).  A floor is needed where the
+    exact result vanishes (e.g. dQ and dK of a one-token sequence)."""
     g, r = to64(gpu), to64(ref)
-    return float(np.linalg.norm((g - r).ravel()) / max(np.linalg.norm(r.ravel()), 1e-300))
+    return float(np.linalg.norm((g - r).ravel()) / max(np.linalg.norm(r.ravel()), floor))
+
+
+def log_errors(case: str, **errs) -> None:
+    """Append measured errors to $PARITY_LOG (JSON lines) when it is set."""
+    import json
+    import os
+    path = os.environ.get("PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": case, **{k: float(v) for k, v in errs.items()}}) + "\n")
 
 
 def max_abs(gpu, ref) -> float:

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from parity_utils import LSE_TOL, REL_TOL, bytes_equal, max_abs, rel_fro, run_path
+from parity_utils import LSE_TOL, REL_TOL, bytes_equal, log_errors, max_abs, rel_fro, run_path
 from ulysses_inputs import WORKLOADS, draw_seq_inputs
 
 pytestmark = pytest.mark.gpu
@@ -36,8 +36,14 @@ def _attn_case(uly, S, B, N, Hq, Hkv, d, dtype, causal, cu, seed=0):
     torch.cuda.synchronize()
     assert uly.ulysses_get_device_status()[0] == 0
     dq_r, dk_r, dv_r, o_r, lse_r = oracle.attn_bwd(q, k, v, do, causal=causal, cu_seqlens=cu)
-    errs = dict(o=rel_fro(o, o_r), dq=rel_fro(dq, dq_r), dk=rel_fro(dk, dk_r), dv=rel_fro(dv, dv_r))
+    # with one token dS = dP - D vanishes: dQ and dK are exactly 0, so their
+    # error is measured against the size of the other gradients instead
+    floor = float(np.linalg.norm(dv_r)) if N == 1 else 1e-300
+    errs = dict(o=rel_fro(o, o_r), dq=rel_fro(dq, dq_r, floor), dk=rel_fro(dk, dk_r, floor),
+                dv=rel_fro(dv, dv_r))
     lse_err = max_abs(lse, lse_r)
+    log_errors(f"attn S{S} B{B} N{N} Hq{Hq} Hkv{Hkv} d{d} {tag} causal{int(causal)} docs{0 if cu is None else len(cu) - 1}",
+               lse_max_abs=lse_err, **errs)
     for name, e in errs.items():
         assert e <= REL_TOL[tag], (name, e, errs, lse_err)
     assert lse_err <= LSE_TOL[tag], (lse_err, errs)
