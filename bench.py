@@ -361,7 +361,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_4b_n65536")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--oracle-rows", type=int, default=384)
+    ap.add_argument("--oracle-rows", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
