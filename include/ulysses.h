@@ -52,7 +52,8 @@ typedef enum {
     ULY_ERR_OVERLAP = 4,     /* input and output buffers overlap */
     ULY_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
     ULY_ERR_TIMEOUT = 6,     /* a device-side bounded wait ran out */
-    ULY_ERR_WORKSPACE = 7    /* workspace missing or smaller than required */
+    ULY_ERR_WORKSPACE = 7,   /* workspace missing or smaller than required */
+    ULY_ERR_SCRATCH_LIMIT = 8 /* sizes need more scratch than ulysses_attn_bwd_noalloc has */
 } uly_status;
 
 typedef enum { ULY_BF16 = 0, ULY_FP32 = 1 } uly_dtype;
@@ -149,6 +150,36 @@ uly_status ulysses_attn_bwd(const void *q, const void *k, const void *v, const v
                             int32_t num_shards, int32_t causal, const int32_t *cu_seqlens_host,
                             int32_t num_docs, float softmax_scale, uly_dtype dtype, void *workspace,
                             size_t workspace_bytes, void *stream);
+
+/*
+ * ulysses_attn_bwd without a workspace, for callers that cannot allocate
+ * device memory: code running inside an allocator's own hooks, a process
+ * whose device memory pool is fixed up front, a plugin that is handed only
+ * the tensors it works on, or a latency-critical path that must not take the
+ * allocator's locks.  The pages have no counterpart: the method itself does
+ * not care where scratch lives.
+ *
+ * Same arguments and results as ulysses_attn_bwd, minus workspace.  The fp32
+ * scratch (lse*log2(e), D, the dQ accumulator, the cu_seqlens copy) lives in
+ * one fixed 64 MiB device array inside the library; every GPU that loads
+ * this part of the library holds those 64 MiB until the process exits.
+ * Sizes whose scratch (ulysses_attn_workspace_size(..., for_bwd=1, ...))
+ * exceeds 64 MiB return ULY_ERR_SCRATCH_LIMIT and launch nothing; for bf16
+ * that is about 129,000 (shard x batch x query-head x padded-row) rows, e.g.
+ * N = 8192 with 8 local query heads and 1 shard fits.
+ * The call allocates nothing (no cudaMalloc, no allocating library routine).
+ * The first call on a device looks up the array's device address; make that
+ * first call before any stream capture.  All calls share the array: calls
+ * that overlap on the GPU (other streams, other threads) race and must not
+ * be issued; sequential calls are safe because each one rewrites or clears
+ * every scratch byte it reads.
+ */
+uly_status ulysses_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                                    const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                                    int64_t B, int64_t N, int32_t Hq_local, int32_t Hkv_local,
+                                    int32_t d, int32_t num_shards, int32_t causal,
+                                    const int32_t *cu_seqlens_host, int32_t num_docs,
+                                    float softmax_scale, uly_dtype dtype, void *stream);
 
 /* ------------------------------------------------------------ diagnostics */
 

@@ -27,11 +27,12 @@ ULY_OK = 0
 ULY_BF16 = 0
 ULY_FP32 = 1
 _STATUS = {0: "ULY_OK", 1: "ULY_ERR_INVALID_ARG", 2: "ULY_ERR_UNSUPPORTED", 3: "ULY_ERR_MISALIGNED",
-           4: "ULY_ERR_OVERLAP", 5: "ULY_ERR_CUDA", 6: "ULY_ERR_TIMEOUT", 7: "ULY_ERR_WORKSPACE"}
+           4: "ULY_ERR_OVERLAP", 5: "ULY_ERR_CUDA", 6: "ULY_ERR_TIMEOUT", 7: "ULY_ERR_WORKSPACE",
+           8: "ULY_ERR_SCRATCH_LIMIT"}
 
 # every symbol include/ulysses.h declares
 EXPORTED = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_workspace_size",
-            "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_get_device_status",
+            "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc", "ulysses_get_device_status",
             "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout",
             "ulysses_status_string", "ulysses_version")
 
@@ -69,6 +70,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.ulysses_attn_workspace_size.restype = sz
     lib.ulysses_attn_fwd.argtypes = [vp] * 5 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp, sz, vp]
     lib.ulysses_attn_bwd.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp, sz, vp]
+    lib.ulysses_attn_bwd_noalloc.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp]
     lib.ulysses_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.ulysses_set_wait_limit_ns.argtypes = [u64]
     lib.ulysses_selftest_wait_timeout.argtypes = [u64, vp]
@@ -76,6 +78,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.ulysses_status_string.restype = ctypes.c_char_p
     lib.ulysses_version.restype = i32
     for name in ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_fwd", "ulysses_attn_bwd",
+                 "ulysses_attn_bwd_noalloc",
                  "ulysses_get_device_status", "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout"):
         getattr(lib, name).restype = i32
     _lib = lib
@@ -189,6 +192,23 @@ def ulysses_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = True,
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, N, Hq, Hkv, d, S, int(bool(causal)), cu_p, nd,
         float(softmax_scale), _dt(q), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
+    return dq, dk, dv
+
+
+def ulysses_attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = True,
+                             cu_seqlens: Optional[Sequence[int]] = None, softmax_scale: float = 0.0,
+                             stream=None):
+    """Attention backward without a workspace, for callers that cannot
+    allocate device memory; its scratch is a fixed 64 MiB array inside the
+    library (see include/ulysses.h for the limits and the ordering rule)."""
+    _dev(q, k, v, o, lse, dout, dq, dk, dv)
+    S, B, N, Hq, d = q.shape
+    Hkv = k.shape[3]
+    cu_p, nd, _keep = _cu(cu_seqlens)
+    _check("ulysses_attn_bwd_noalloc", load().ulysses_attn_bwd_noalloc(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, N, Hq, Hkv, d, S, int(bool(causal)), cu_p, nd,
+        float(softmax_scale), _dt(q), _stream(stream)))
     return dq, dk, dv
 
 

@@ -397,6 +397,8 @@ const char *ulysses_status_string(uly_status status)
         return "device-side wait timed out";
     case ULY_ERR_WORKSPACE:
         return "workspace missing or too small";
+    case ULY_ERR_SCRATCH_LIMIT:
+        return "sizes exceed the fixed scratch of the no-allocation entry point";
     }
     return "unknown status";
 }

@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(uly):
 
 def test_version_and_strings(uly):
     assert uly.ulysses_version() == 100
-    for code in range(8):
+    for code in range(9):
         assert uly.ulysses_status_string(code)
     assert uly.ulysses_status_string(0) == "ok"
 
