@@ -184,12 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *s_full = bars + 5;
     uint64_t *dp_full = bars + 6;
     uint64_t *ds_full = bars + 7;
+    uint64_t *p_full = bars + 13;
     uint64_t *ds_empty = bars + 8;
     uint64_t *dq_full = bars + 9;
     uint64_t *dq_empty = bars + 10;
     uint64_t *dkv_done = bars + 11;
     uint64_t *drain = bars + 12;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = warp_id();
@@ -212,10 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_it = p.G * n_m;
 
     if (warp == 8 && lane == 0) {
-        for (int i = 0; i < 13; ++i)
+        for (int i = 0; i < 14; ++i)
             mbar_init(&bars[i], 1);
-        mbar_init(ds_full, kBN);
-        mbar_init(dq_empty, kBM);
+        mbar_init(ds_full, 2 * kBN);   // both compute warpgroups
+        mbar_init(p_full, 2 * kBN);
+        mbar_init(dq_empty, 2 * kBM);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -270,51 +272,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------ MMA issuer
+        // Issue order per iteration it:  dP(it) | dV(it) | S(it+1) | dK(it), dQ(it)
+        // so the P part of it+1 and the dS part of it run on the compute
+        // warpgroups while the tensor pipe works on the neighbours.
         if (lane == 0) {
             const uint32_t id_kk = idesc_bf16(128, 128, false, false);  // both K-major
             const uint32_t id_kmn = idesc_bf16(128, 128, false, true);  // B MN-major
             const uint32_t id_mnmn = idesc_bf16(128, 128, true, true);  // A and B MN-major
             const uint32_t sK = smem_u32(smem + BwdSmem::kK), sV = smem_u32(smem + BwdSmem::kV);
             const uint32_t sdS = smem_u32(smem + BwdSmem::kdS);
-            bool ok = mbar_wait(kv_full, 0, p.w, 0x61);
-            for (int it = 0; ok && it < n_it; ++it) {
-                const int slot = it & 1;
-                const uint32_t sQ = smem_u32(smem + BwdSmem::kQ + slot * kTile);
-                const uint32_t sdO = smem_u32(smem + BwdSmem::kdO + slot * kTile);
-                if (!mbar_wait(&q_full[slot], (it >> 1) & 1, p.w, 0x62)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // S^T = K Q^T
+            auto issue_s = [&](int it) {  // S^T = K Q^T
+                const uint32_t sQ = smem_u32(smem + BwdSmem::kQ + (it & 1) * kTile);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
                     mma_ss(tS, desc_sw128(sK + off, 16, 1024), desc_sw128(sQ + off, 16, 1024), id_kk, kk > 0);
                 }
                 mma_commit(s_full);
+            };
+            bool ok = mbar_wait(kv_full, 0, p.w, 0x61) && (n_it == 0 || mbar_wait(&q_full[0], 0, p.w, 0x62));
+            if (ok && n_it > 0) {
+                tc_fence_after();
+                issue_s(0);
+            }
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int slot = it & 1;
+                const uint32_t sQ = smem_u32(smem + BwdSmem::kQ + slot * kTile);
+                const uint32_t sdO = smem_u32(smem + BwdSmem::kdO + slot * kTile);
+                // dP^T = V dO^T into the dP/dQ columns, once dQ(it-1) has been read out
                 if (it > 0 && !mbar_wait(dq_empty, (it - 1) & 1, p.w, 0x63)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // dP^T = V dO^T
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
                     mma_ss(tdP, desc_sw128(sV + off, 16, 1024), desc_sw128(sdO + off, 16, 1024), id_kk, kk > 0);
                 }
                 mma_commit(dp_full);
-                if (!mbar_wait(ds_full, it & 1, p.w, 0x64)) {
+                // dV += P^T dO   (A = P^T in TMEM: query columns 0-63 at S cols 0-31,
+                // 64-127 at S cols 64-95; B = dO, d contiguous)
+                if (!mbar_wait(p_full, it & 1, p.w, 0x64)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // dV += P^T dO   (A = P^T in TMEM, B = dO, d contiguous)
 #pragma unroll
                 for (int kk = 0; kk < kBM / 16; ++kk)
-                    mma_ts(tdV, tS + kk * 8, desc_sw128(sdO + kk * 2048, kChunk, 1024), id_kmn,
+                    mma_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, desc_sw128(sdO + kk * 2048, kChunk, 1024), id_kmn,
                            (it > 0 || kk > 0) ? 1u : 0u);
+                // next S^T (overwrites P^T(it), which dV(it) above has already consumed in order)
+                if (it + 1 < n_it) {
+                    if (!mbar_wait(&q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, p.w, 0x65)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_s(it + 1);
+                }
+                if (!mbar_wait(ds_full, it & 1, p.w, 0x66)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 // dK += dS^T Q   (A = dS^T K-major, B = Q, d contiguous)
 #pragma unroll
                 for (int kk = 0; kk < kBM / 16; ++kk) {
@@ -337,47 +358,69 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(drain);
             mbar_wait(drain, 0, p.w, 0x6f);
         }
-    } else if (warp < 4) {
-        // ------------------------------------------------ P^T / dS^T warpgroup
-        const int j = warp * 32 + lane;  // key row in the tile == TMEM lane
+    } else {
+        // ------------------------------------------------ compute warpgroups
+        // warps 0-3 take query columns 0-63, warps 4-7 columns 64-127, of the
+        // same 128 key rows (TMEM lane = key row).  They also read each dQ
+        // partial (TMEM lane = query row, d columns of their half) and reduce
+        // it into the accumulator, and write dK/dV at the end.
+        const int hf = warp >> 2;                  // column half
+        const int q4 = warp & 3;                   // TMEM lane quarter
+        const int j = q4 * 32 + lane;              // key row / dQ query row in the tile
         const int64_t key = kv0 + j;
-        int64_t lo = 0, hi = 0;  // rows that may attend to this key: [lo, hi)
+        int64_t lo = 0, hi = 0;                    // rows that may attend to this key: [lo, hi)
         if (key < p.N) {
             doc_range(p, key, lo, hi);
             if (p.causal)
                 lo = key;
         }
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
         const float sl2 = p.scale_log2;
-        uint8_t *ds_row = smem + BwdSmem::kdS + j * 128;
+        uint8_t *ds_chunk = smem + BwdSmem::kdS + hf * kChunk + j * 128;
+        const int c0 = hf * 64;                    // first query column / d column of this half
         bool ok = true;
+        auto reduce_dq = [&](int it) {             // dQ(it) partial -> accumulator
+            const int h = kvh * p.G + it / n_m;
+            const int m = m_lo + it % n_m;
+            uint32_t x[64];
+            tmem_ld32p(tdP + lane_off + c0, x);
+            tmem_ld32p(tdP + lane_off + c0 + 32, x + 32);
+            tmem_ld_wait();
+            tmem_ld_fence32p(x);
+            tmem_ld_fence32p(x + 32);
+            tc_fence_before();
+            mbar_arrive(dq_empty);
+            if (static_cast<int64_t>(m) * kBM + j < p.N) {
+                float *base = p.dq_acc +
+                              (((static_cast<int64_t>(sb) * p.Hq + h) * (p.Npad / kBM) + m) * 32 + c0 / 4) * (kBM * 4) +
+                              j * 4;
+#pragma unroll
+                for (int g = 0; g < 16; ++g)
+                    red_add_v4(base + g * (kBM * 4), __uint_as_float(x[4 * g]), __uint_as_float(x[4 * g + 1]),
+                               __uint_as_float(x[4 * g + 2]), __uint_as_float(x[4 * g + 3]));
+            }
+        };
         for (int it = 0; it < n_it; ++it) {
             const int slot = it & 1;
             const int64_t q0 = static_cast<int64_t>(m_lo + it % n_m) * kBM;
-            const float *lse_s = reinterpret_cast<const float *>(smem + BwdSmem::kLse + slot * 512);
-            const float *D_s = reinterpret_cast<const float *>(smem + BwdSmem::kDv + slot * 512);
-            if (!mbar_wait_warp(s_full, it & 1, p.w, 0x71)) {
-                ok = false;
-                break;
-            }
-            // lse and D of this query tile were delivered with Q (same barrier)
-            if (!mbar_wait_warp(&q_full[slot], (it >> 1) & 1, p.w, 0x72)) {
+            const float *lse_s = reinterpret_cast<const float *>(smem + BwdSmem::kLse + slot * 512) + c0;
+            const float *D_s = reinterpret_cast<const float *>(smem + BwdSmem::kDv + slot * 512) + c0;
+            if (!mbar_wait_warp(s_full, it & 1, p.w, 0x71) ||
+                !mbar_wait_warp(&q_full[slot], (it >> 1) & 1, p.w, 0x72)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t u[kBM];
-#pragma unroll
-            for (int cb = 0; cb < kBM; cb += 32)
-                tmem_ld32p(tS + lane_off + cb, u + cb);
+            uint32_t u[64];
+            tmem_ld32p(tS + lane_off + c0, u);
+            tmem_ld32p(tS + lane_off + c0 + 32, u + 32);
             tmem_ld_wait();
+            tmem_ld_fence32p(u);
+            tmem_ld_fence32p(u + 32);
+            const bool full = (q0 + c0 >= lo) && (q0 + c0 + 64 <= hi);
+            uint32_t pk[32];
 #pragma unroll
-            for (int cb = 0; cb < kBM; cb += 32)
-                tmem_ld_fence32p(u + cb);
-            const bool full = (q0 >= lo) && (q0 + kBM <= hi);
-            uint32_t pk[kBM / 2];
-#pragma unroll
-            for (int c = 0; c < kBM; c += 4) {
+            for (int c = 0; c < 64; c += 4) {
                 const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + c);
                 float pv[4];
                 pv[0] = ex2_approx(fmaf(__uint_as_float(u[c + 0]), sl2, -l4.x));
@@ -387,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!full) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int64_t row = q0 + c + e;
+                        const int64_t row = q0 + c0 + c + e;
                         if (row < lo || row >= hi)
                             pv[e] = 0.f;
                     }
@@ -395,22 +438,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[c / 2] = pack_bf16x2(pv[0], pv[1]);
                 pk[c / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
             }
-            tmem_st32p(tS + lane_off, pk);
-            tmem_st32p(tS + lane_off + 32, pk + 32);
-            // dS^T needs the shared buffer the previous iteration's dK/dQ products read
-            if (it > 0 && !mbar_wait_warp(ds_empty, (it - 1) & 1, p.w, 0x73)) {
-                ok = false;
-                break;
+            // P^T of this half into its own S columns (c0 .. c0+31)
+            tmem_st32p(tS + lane_off + c0, pk);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(p_full);
+            // the previous iteration's dQ partial (frees the dP/dQ columns)
+            if (it > 0) {
+                if (!mbar_wait_warp(dq_full, (it - 1) & 1, p.w, 0x73)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                reduce_dq(it - 1);
             }
-            if (!mbar_wait_warp(dp_full, it & 1, p.w, 0x74)) {
+            // dS^T needs the shared buffer the previous dK/dQ products read
+            if ((it > 0 && !mbar_wait_warp(ds_empty, (it - 1) & 1, p.w, 0x74)) ||
+                !mbar_wait_warp(dp_full, it & 1, p.w, 0x75)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
 #pragma unroll
-            for (int cb = 0; cb < kBM; cb += 32) {
+            for (int cb = 0; cb < 64; cb += 32) {
                 uint32_t dp[32];
-                tmem_ld32p(tdP + lane_off + cb, dp);
+                tmem_ld32p(tdP + lane_off + c0 + cb, dp);
                 tmem_ld_wait();
                 tmem_ld_fence32p(dp);
                 uint32_t dsp[16];
@@ -425,38 +477,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dsp[c / 2] = pack_bf16x2(ds0, ds1);
                     dsp[c / 2 + 1] = pack_bf16x2(ds2, ds3);
                 }
-                // columns cb..cb+31 = four 16-byte units of the swizzled row
+                // columns c0+cb .. +31 = four 16-byte units of this half's swizzled row
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int unit = (cb / 8) + q;  // 0..15
-                    const int chunk = unit >> 3;
-                    const int phys = (unit & 7) ^ (j & 7);
-                    *reinterpret_cast<uint4 *>(ds_row + chunk * kChunk + phys * 16) =
-                        make_uint4(dsp[4 * q], dsp[4 * q + 1], dsp[4 * q + 2], dsp[4 * q + 3]);
+                for (int qd = 0; qd < 4; ++qd) {
+                    const int unit = (cb / 8) + qd;  // 0..7 within the 64-column chunk
+                    const int phys = unit ^ (j & 7);
+                    *reinterpret_cast<uint4 *>(ds_chunk + phys * 16) =
+                        make_uint4(dsp[4 * qd], dsp[4 * qd + 1], dsp[4 * qd + 2], dsp[4 * qd + 3]);
                 }
             }
             fence_async_smem();
-            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(ds_full);
         }
+        if (ok && n_it > 0) {
+            if (mbar_wait_warp(dq_full, (n_it - 1) & 1, p.w, 0x76)) {
+                tc_fence_after();
+                reduce_dq(n_it - 1);
+            } else {
+                ok = false;
+            }
+        }
         if (!ok)
             *abort_flag = 1;
-        // ---- dK, dV epilogue ----
+        // ---- dK, dV epilogue: key row j, d columns c0 .. c0+63 ----
         if (mbar_wait_warp(dkv_done, 0, p.w, 0x78) && ok) {
             tc_fence_after();
             const bool store = key < p.N;
-            uint16_t *dkp = p.dk + ((static_cast<int64_t>(sb) * p.N + (store ? key : 0)) * p.Hkv + kvh) * kD;
-            uint16_t *dvp = p.dv + ((static_cast<int64_t>(sb) * p.N + (store ? key : 0)) * p.Hkv + kvh) * kD;
+            const int64_t rowoff = ((static_cast<int64_t>(sb) * p.N + (store ? key : 0)) * p.Hkv + kvh) * kD + c0;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
-                const uint32_t src = which ? tdK : tdV;
+                const uint32_t src = (which ? tdK : tdV) + lane_off + c0;
                 const float f = which ? p.scale : 1.f;
-                uint16_t *dst = which ? dkp : dvp;
+                uint16_t *dst = (which ? p.dk : p.dv) + rowoff;
 #pragma unroll
-                for (int cb = 0; cb < kD; cb += 32) {
+                for (int cb = 0; cb < 64; cb += 32) {
                     uint32_t x[32];
-                    tmem_ld32p(src + lane_off + cb, x);  // warp-collective: all lanes
+                    tmem_ld32p(src + cb, x);  // warp-collective: all lanes
                     tmem_ld_wait();
                     tmem_ld_fence32p(x);
                     uint32_t o16[16];
@@ -474,41 +531,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else {
-        // ------------------------------------------------ dQ warpgroup
-        const int r = (warp - 4) * 32 + lane;  // query row within the tile
-        const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
-        bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
-            const int h = kvh * p.G + it / n_m;
-            const int m = m_lo + it % n_m;
-            if (!mbar_wait_warp(dq_full, it & 1, p.w, 0x81)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t x[kD];
-#pragma unroll
-            for (int cb = 0; cb < kD; cb += 32)
-                tmem_ld32p(tdP + lane_off + cb, x + cb);
-            tmem_ld_wait();
-#pragma unroll
-            for (int cb = 0; cb < kD; cb += 32)
-                tmem_ld_fence32p(x + cb);
-            tc_fence_before();
-            mbar_arrive(dq_empty);
-            if (static_cast<int64_t>(m) * kBM + r < p.N) {
-                float *base = p.dq_acc + (((static_cast<int64_t>(sb) * p.Hq + h) * (p.Npad / kBM) + m) * 32) *
-                                             (kBM * 4) +
-                              r * 4;
-#pragma unroll
-                for (int g = 0; g < 32; ++g)
-                    red_add_v4(base + g * (kBM * 4), __uint_as_float(x[4 * g]), __uint_as_float(x[4 * g + 1]),
-                               __uint_as_float(x[4 * g + 2]), __uint_as_float(x[4 * g + 3]));
-            }
-        }
-        if (!ok)
-            *abort_flag = 1;
     }
 
     __syncwarp();
