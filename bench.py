@@ -56,9 +56,12 @@ def _pairs(N: int, cu) -> int:
     return int((L * (L + 1) // 2).sum())
 
 
-def _workload(name):
+def _workload(name, seq_len=None):
+    import dataclasses
     from ulysses_inputs import WORKLOADS, cu_seqlens_from_lengths, doc_lengths
     w = WORKLOADS[name]
+    if seq_len:
+        w = dataclasses.replace(w, N=int(seq_len))
     cu = cu_seqlens_from_lengths(doc_lengths(w.N, w.P, seed=3)) if w.packed_docs else None
     return w, cu
 
@@ -120,6 +123,23 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# -------------------------------------------------------- multi-rank logic
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The slowest rank's time (all ranks of a replica run do equal work)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(world: int, flops_per_rank_step: float, ms_per_step: float) -> float:
+    """TFLOP/s of all ranks together: every replica processes one step per
+    ms_per_step (the max over ranks)."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------- our arm
 def run_ours(args, rank, world, dist):
     import torch
@@ -127,7 +147,7 @@ def run_ours(args, rank, world, dist):
     from ulysses_inputs import draw_seq_inputs
 
     uly.load(build_if_missing=True)
-    w, cu = _workload(args.workload)
+    w, cu = _workload(args.workload, args.seq_len)
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     P, S, B, N, d = w.P, w.shards_timed, w.B, w.N, w.d
@@ -201,10 +221,7 @@ def run_ours(args, rank, world, dist):
         raise RuntimeError(f"device status {st} at site {site:#x} in the timed region")
     phase = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(args.steps)]
     ph = [statistics.mean(p[j] for p in phase) for j in range(5)]
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
 
     # ---- end to end: host buffers in pinned memory, copies inside the timed region
     pin = lambda x: torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -229,15 +246,12 @@ def run_ours(args, rank, world, dist):
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
 
     fwd_flops, bwd_flops = _flops(w, cu)
     step_flops = fwd_flops + bwd_flops
     ms = elapsed_ms / args.steps
-    value = world * step_flops / (ms * 1e-3) / 1e12
+    value = whole_job_throughput(world, step_flops, ms)
     hbm, tc_burst, tc_sus, src = _peaks()
     swap_bytes = 2 * sum(x.numel() * x.element_size() for x in (q, k, v, do))
     if full:
@@ -262,7 +276,7 @@ def run_ours(args, rank, world, dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded N(0,1) Q/K/V/dO of the workload's shapes)",
-        "config": {"workload": args.workload, "B": B, "N": N, "P": P, "Hq": w.Hq, "Hkv": w.Hkv, "d": d,
+        "config": {"workload": args.workload + (f" (N overridden to {N})" if args.seq_len else ""), "B": B, "N": N, "P": P, "Hq": w.Hq, "Hkv": w.Hkv, "d": d,
                    "causal": w.causal, "head_shards_timed": S, "packed_docs": w.packed_docs,
                    "l2": "no flush: inputs larger than L2 (Q,K,V,dO %.2f GiB per step)" % (
                        sum(x.numel() * x.element_size() for x in (q, k, v, do)) / 2**30),
@@ -282,7 +296,7 @@ def run_ours(args, rank, world, dist):
                      "frac": round(bwd_tflops / tc_sus, 3), "traffic": traffic,
                      "peak_source": f"{src} bf16 sustained (MEASURED_PEAKS.json)" if src == "measured"
                      else "fallback 1.7 PFLOP/s sustained"},
-        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+        "e2e": {"value": round(whole_job_throughput(world, step_flops, e2e_ms), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
         "clocks": clk.summary(),
         "gpu_launches": args.steps * ((8 if full else 4) + 1 + 3),
@@ -327,7 +341,7 @@ def oracle_sample(w, cu, heads, rows_per_step, seed):
 
 def run_reference(args, rank, world):
     import oracle
-    w, cu = _workload(args.workload)
+    w, cu = _workload(args.workload, args.seq_len)
     oracle.build()
     cores = oracle.num_threads()
     heads = oracle_inputs(w, args.seed)
@@ -361,6 +375,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_4b_n65536")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="override the workload's N (profiling smaller cases of the same kernels)")
     ap.add_argument("--oracle-rows", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -381,7 +397,7 @@ def main():
         dist.init_process_group("nccl")
     line = run_ours(args, rank, world, dist)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        w, cu = _workload(args.workload)
+        w, cu = _workload(args.workload, args.seq_len)
         import oracle
         oracle.build()
         heads = oracle_inputs(w, args.seed)
