@@ -196,11 +196,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = warp_id();
     const int lane = lane_id();
 
-    // ---- work unit: key tiles with the most query tiles first ----
-    const int64_t per_n = p.SB * p.Hkv;
-    const int n_blk = static_cast<int>(blockIdx.x / per_n);
-    const int kvh = static_cast<int>(blockIdx.x % p.Hkv);
-    const int sb = static_cast<int>((blockIdx.x / p.Hkv) % p.SB);
+    // ---- work unit: problem-major (all resident CTAs share one (shard*batch,
+    // KV head) problem, so its Q/dO tiles and dQ accumulator stay in L2), key
+    // tiles with the most query tiles first within a problem ----
+    const int n_blk = static_cast<int>(blockIdx.x % p.n_ktiles);
+    const int prob = static_cast<int>(blockIdx.x / p.n_ktiles);
+    const int kvh = prob % p.Hkv;
+    const int sb = prob / p.Hkv;
     const int64_t kv0 = static_cast<int64_t>(n_blk) * kBN;
     const int64_t key_last = (kv0 + kBN - 1 < p.N - 1) ? kv0 + kBN - 1 : p.N - 1;
     int64_t row_lo, row_hi, tmp;
@@ -379,25 +381,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *ds_chunk = smem + BwdSmem::kdS + hf * kChunk + j * 128;
         const int c0 = hf * 64;                    // first query column / d column of this half
         bool ok = true;
-        auto reduce_dq = [&](int it) {             // dQ(it) partial -> accumulator
+        // dQ(it) partial: read out of TMEM (frees the dP/dQ columns), then its
+        // 16 vector reductions are issued in groups of 4 between later work so
+        // the load/store queue never fills in one burst
+        uint32_t xq[64];
+        float *dq_base = nullptr;
+        auto read_dq = [&](int it) {
             const int h = kvh * p.G + it / n_m;
             const int m = m_lo + it % n_m;
-            uint32_t x[64];
-            tmem_ld32p(tdP + lane_off + c0, x);
-            tmem_ld32p(tdP + lane_off + c0 + 32, x + 32);
+            tmem_ld32p(tdP + lane_off + c0, xq);
+            tmem_ld32p(tdP + lane_off + c0 + 32, xq + 32);
             tmem_ld_wait();
-            tmem_ld_fence32p(x);
-            tmem_ld_fence32p(x + 32);
+            tmem_ld_fence32p(xq);
+            tmem_ld_fence32p(xq + 32);
             tc_fence_before();
             mbar_arrive(dq_empty);
-            if (static_cast<int64_t>(m) * kBM + j < p.N) {
-                float *base = p.dq_acc +
-                              (((static_cast<int64_t>(sb) * p.Hq + h) * (p.Npad / kBM) + m) * 32 + c0 / 4) * (kBM * 4) +
-                              j * 4;
+            dq_base = (static_cast<int64_t>(m) * kBM + j < p.N)
+                          ? p.dq_acc +
+                                (((static_cast<int64_t>(sb) * p.Hq + h) * (p.Npad / kBM) + m) * 32 + c0 / 4) *
+                                    (kBM * 4) +
+                                j * 4
+                          : nullptr;
+        };
+        auto reduce_dq_part = [&](int part) {  // groups 4*part .. 4*part+3
+            if (dq_base != nullptr) {
 #pragma unroll
-                for (int g = 0; g < 16; ++g)
-                    red_add_v4(base + g * (kBM * 4), __uint_as_float(x[4 * g]), __uint_as_float(x[4 * g + 1]),
-                               __uint_as_float(x[4 * g + 2]), __uint_as_float(x[4 * g + 3]));
+                for (int g = 4 * part; g < 4 * part + 4; ++g)
+                    red_add_v4(dq_base + g * (kBM * 4), __uint_as_float(xq[4 * g]), __uint_as_float(xq[4 * g + 1]),
+                               __uint_as_float(xq[4 * g + 2]), __uint_as_float(xq[4 * g + 3]));
             }
         };
         for (int it = 0; it < n_it; ++it) {
@@ -450,7 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                reduce_dq(it - 1);
+                read_dq(it - 1);
+                reduce_dq_part(0);
+            } else {
+                dq_base = nullptr;
             }
             // dS^T needs the shared buffer the previous dK/dQ products read
             if ((it > 0 && !mbar_wait_warp(ds_empty, (it - 1) & 1, p.w, 0x74)) ||
@@ -461,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int cb = 0; cb < 64; cb += 32) {
+                reduce_dq_part(1 + cb / 32);
                 uint32_t dp[32];
                 tmem_ld32p(tdP + lane_off + c0 + cb, dp);
                 tmem_ld_wait();
@@ -489,11 +504,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(ds_full);
+            reduce_dq_part(3);
         }
         if (ok && n_it > 0) {
             if (mbar_wait_warp(dq_full, (n_it - 1) & 1, p.w, 0x76)) {
                 tc_fence_after();
-                reduce_dq(n_it - 1);
+                read_dq(n_it - 1);
+#pragma unroll
+                for (int part = 0; part < 4; ++part)
+                    reduce_dq_part(part);
             } else {
                 ok = false;
             }
