@@ -92,15 +92,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = warp_id();
     const int lane = lane_id();
 
-    // ---- work unit (longest query blocks first) ----
-    const int64_t per_m = p.SB * p.Hkv * p.npairs;
+    // ---- work unit: problem-major (resident CTAs share one (shard*batch,
+    // KV head) problem and stream the same K/V tiles through L2), longest
+    // query blocks first within a problem ----
     const int64_t u = blockIdx.x;
-    const int m_blk = p.n_qtiles - 1 - static_cast<int>(u / per_m);
-    int64_t rest = u % per_m;
-    const int pair = static_cast<int>(rest % p.npairs);
-    rest /= p.npairs;
-    const int kvh = static_cast<int>(rest % p.Hkv);
-    const int sb = static_cast<int>(rest / p.Hkv);
+    const int pair = static_cast<int>(u % p.npairs);
+    const int m_blk = p.n_qtiles - 1 - static_cast<int>((u / p.npairs) % p.n_qtiles);
+    const int64_t prob = u / (static_cast<int64_t>(p.npairs) * p.n_qtiles);
+    const int kvh = static_cast<int>(prob % p.Hkv);
+    const int sb = static_cast<int>(prob / p.Hkv);
     const int h0 = kvh * p.G + 2 * pair;
     const bool has1 = (2 * pair + 1) < p.G;
     const int64_t q0 = static_cast<int64_t>(m_blk) * kBM;
@@ -283,18 +283,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cb = 0; cb < kBN; cb += 32)
                     tmem_ld_fence32p(u + cb);
                 const int64_t key0 = static_cast<int64_t>(kt_lo + j) * kBN;
-                if (key0 < lo || key0 + kBN > hi) {
+                const bool masked = key0 < lo || key0 + kBN > hi;
+                if (masked) {
+                    // allowed columns of this tile: [lo_c, hi_c)
+                    const int lo_c = static_cast<int>(max(lo - key0, int64_t(0)));
+                    const int hi_c = static_cast<int>(min(hi - key0, int64_t(kBN)));
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c) {
-                        const int64_t key = key0 + c;
-                        if (key < lo || key >= hi)
+                    for (int c = 0; c < kBN; ++c)
+                        if (c < lo_c || c >= hi_c)
                             u[c] = __float_as_uint(-INFINITY);
-                    }
                 }
-                float mx = __uint_as_float(u[0]);
+                // row maximum with 8 independent partial maxima (short chains)
+                float pm[8];
 #pragma unroll
-                for (int c = 1; c < kBN; ++c)
-                    mx = fmaxf(mx, __uint_as_float(u[c]));
+                for (int e = 0; e < 8; ++e)
+                    pm[e] = __uint_as_float(u[e]);
+#pragma unroll
+                for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        pm[e] = fmaxf(pm[e], __uint_as_float(u[c + e]));
+                const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
                 const float m_cand = mx * p.scale_log2;
                 float alpha = 1.f;
                 bool rescale = false;
@@ -305,14 +315,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l *= alpha;
                 const float m_use = (m == -INFINITY) ? 0.f : m;
-                float rs = 0.f;
+                const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+                const float2 nm2 = make_float2(-m_use, -m_use);
+                float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
+                // p = 2^(s * scale * log2(e) - m) on the SFU (masked scores are
+                // -inf and give exactly 0); the scale-and-shift and the row sum
+                // run as packed f32x2 pairs, the sum in four independent chains
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    const float pv = ex2_approx(fmaf(__uint_as_float(u[c]), p.scale_log2, -m_use));
-                    rs += pv;
-                    u[c] = __float_as_uint(pv);
+                for (int c = 0; c < kBN; c += 2) {
+                    const float2 x = ffma2(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2, nm2);
+                    const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    rs2[(c >> 1) & 3] = fadd2(rs2[(c >> 1) & 3], pv);
+                    u[c] = __float_as_uint(pv.x);
+                    u[c + 1] = __float_as_uint(pv.y);
                 }
-                l += rs;
+                const float2 r01 = fadd2(rs2[0], rs2[1]), r23 = fadd2(rs2[2], rs2[3]);
+                const float2 r = fadd2(r01, r23);
+                l += r.x + r.y;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t pk[32];

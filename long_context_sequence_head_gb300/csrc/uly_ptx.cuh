@@ -365,27 +365,6 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b)
     return d;
 }
 
-// 2^x on the FMA/INT pipes for a pair of arguments, x >= -126 after
-// clamping.  n = round(x) comes from adding and subtracting 1.5 * 2^23
-// (n then sits in the low mantissa bits of the sum), f = x - n lies in
-// [-1/2, 1/2], 2^f is a cubic minimax fit (max relative error 7.5e-5; the
-// fit is derived in exp2_poly_fit.py) and n is added to its exponent bits.
-__device__ __forceinline__ float2 exp2_poly2(float2 x)
-{
-    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-    x.x = fmaxf(x.x, -126.0f);
-    x.y = fmaxf(x.y, -126.0f);
-    const float2 t = fadd2(x, make_float2(kMagic, kMagic));
-    const float2 n = fadd2(t, make_float2(-kMagic, -kMagic));
-    const float2 f = fadd2(x, make_float2(-n.x, -n.y));
-    float2 p = ffma2(make_float2(0.055171494f, 0.055171494f), f, make_float2(0.242610938f, 0.242610938f));
-    p = ffma2(p, f, make_float2(0.693260994f, 0.693260994f));
-    p = ffma2(p, f, make_float2(0.999928085f, 0.999928085f));
-    const int ex = __float_as_int(p.x) + (__float_as_int(t.x) << 23);
-    const int ey = __float_as_int(p.y) + (__float_as_int(t.y) << 23);
-    return make_float2(__int_as_float(ex), __int_as_float(ey));
-}
-
 __device__ __forceinline__ uint32_t elect_one_sync()
 {
     uint32_t pred = 0;
