@@ -19,15 +19,15 @@
 //                accumulator with coalesced vector reductions.
 //   dq_convert : fp32 accumulator * scale -> bf16 dQ in the head layout.
 //
-// bwd_main warp roles (320 threads):
-//   warps 0-3 : thread = key row j (TMEM lane).  S^T row -> P^T (bf16, into
-//               TMEM for the dV product), dP^T row -> dS^T (bf16, into
-//               shared memory for the dK and dQ products); final dK/dV
-//               epilogue.
-//   warps 4-7 : thread = query row of the current tile; reads the dQ partial
-//               out of TMEM and reduces it into global memory.
-//   warp  8   : TMA producer (K, V once; Q, dO, lse, D per iteration, 2 stages)
-//   warp  9   : tcgen05.mma issuer and TMEM owner.
+// bwd_main warp roles (576 threads):
+//   warps 0-15: 4 column quarters x 4 TMEM lane quarters.  Thread = key row j
+//               (TMEM lane) for 32 of the 128 query columns: S^T -> P^T (bf16,
+//               into TMEM for the dV product), dP^T -> dS^T (bf16, into shared
+//               memory for the dK and dQ products).  The same warps read their
+//               32 d-columns of each dQ partial (TMEM lane = query row) and
+//               reduce them into global memory, and write dK/dV at the end.
+//   warp  16  : TMA producer (K, V once; Q, dO, lse, D per iteration, 2 stages)
+//   warp  17  : tcgen05.mma issuer and TMEM owner.
 // TMEM (512 columns): S^T/P^T | dP^T, later dQ | dV | dK.
 // Per (key tile, query tile) the MMAs are S^T = K Q^T, dP^T = V dO^T,
 // dV += P^T dO, dK += dS^T Q, dQ = dS K.
@@ -41,7 +41,9 @@ constexpr int kBN = 128;  // keys per tile
 constexpr int kD = 128;
 constexpr int kTile = kBM * kD * 2;  // 32 KB
 constexpr int kChunk = 128 * 64 * 2; // 16 KB
-constexpr int kThreads = 320;
+constexpr int kCompWarps = 16;                  // 4 column quarters x 4 TMEM lane quarters
+constexpr int kProdWarp = kCompWarps, kMmaWarp = kCompWarps + 1;
+constexpr int kThreads = (kCompWarps + 2) * 32;  // 576
 
 struct BwdSmem {
     static constexpr int kK = 0;
@@ -214,16 +216,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_m = static_cast<int>((row_hi - 1) / kBM) - m_lo + 1;
     const int n_it = p.G * n_m;
 
-    if (warp == 8 && lane == 0) {
+    if (warp == kProdWarp && lane == 0) {
         for (int i = 0; i < 14; ++i)
             mbar_init(&bars[i], 1);
-        mbar_init(ds_full, 2 * kBN);   // both compute warpgroups
-        mbar_init(p_full, 2 * kBN);
-        mbar_init(dq_empty, 2 * kBM);
+        mbar_init(ds_full, kCompWarps * 32);  // every compute thread
+        mbar_init(p_full, kCompWarps * 32);
+        mbar_init(dq_empty, kCompWarps * 32);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tbase = *tmem_slot;
     const uint32_t tS = tbase, tdP = tbase + 128, tdV = tbase + 256, tdK = tbase + 384;
 
-    if (warp == 8) {
+    if (warp == kProdWarp) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tm_q);
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait(&q_full[it & 1], (it >> 1) & 1, p.w, 0x5f);
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issuer
         // Issue order per iteration it:  dP(it) | dV(it) | S(it+1) | dK(it), dQ(it)
         // so the P part of it+1 and the dS part of it run on the compute
@@ -313,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss(tdP, desc_sw128(sV + off, 16, 1024), desc_sw128(sdO + off, 16, 1024), id_kk, kk > 0);
                 }
                 mma_commit(dp_full);
-                // dV += P^T dO   (A = P^T in TMEM: query columns 0-63 at S cols 0-31,
-                // 64-127 at S cols 64-95; B = dO, d contiguous)
+                // dV += P^T dO   (A = P^T in TMEM: query columns 32c..32c+31 packed
+                // at S cols 32c..32c+15; B = dO, d contiguous)
                 if (!mbar_wait(p_full, it & 1, p.w, 0x64)) {
                     ok = false;
                     break;
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kBM / 16; ++kk)
-                    mma_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, desc_sw128(sdO + kk * 2048, kChunk, 1024), id_kmn,
+                    mma_ts(tdV, tS + (kk >> 1) * 32 + (kk & 1) * 8, desc_sw128(sdO + kk * 2048, kChunk, 1024), id_kmn,
                            (it > 0 || kk > 0) ? 1u : 0u);
                 // next S^T (overwrites P^T(it), which dV(it) above has already consumed in order)
                 if (it + 1 < n_it) {
@@ -361,12 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(drain, 0, p.w, 0x6f);
         }
     } else {
-        // ------------------------------------------------ compute warpgroups
-        // warps 0-3 take query columns 0-63, warps 4-7 columns 64-127, of the
-        // same 128 key rows (TMEM lane = key row).  They also read each dQ
-        // partial (TMEM lane = query row, d columns of their half) and reduce
-        // it into the accumulator, and write dK/dV at the end.
-        const int hf = warp >> 2;                  // column half
+        // ------------------------------------------------ compute warps
+        // Warp w owns query columns 32*cq .. 32*cq+31 (cq = w / 4) of the key
+        // rows in TMEM lane quarter w % 4 (TMEM lane = key row).  It also reads
+        // its 32 d-columns of each dQ partial (TMEM lane = query row) and
+        // reduces them into the accumulator, and writes dK/dV at the end.
+        const int cq = warp >> 2;                  // column quarter
         const int q4 = warp & 3;                   // TMEM lane quarter
         const int j = q4 * 32 + lane;              // key row / dQ query row in the tile
         const int64_t key = kv0 + j;
@@ -377,23 +379,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lo = key;
         }
         const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-        const float sl2 = p.scale_log2;
-        uint8_t *ds_chunk = smem + BwdSmem::kdS + hf * kChunk + j * 128;
-        const int c0 = hf * 64;                    // first query column / d column of this half
+        const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+        const int c0 = cq * 32;                    // first query column / d column of this warp
+        // dS^T row j, columns c0..c0+31: four 16-byte units of one 64-column chunk
+        uint8_t *ds_row = smem + BwdSmem::kdS + (cq >> 1) * kChunk + j * 128;
         bool ok = true;
-        // dQ(it) partial: read out of TMEM (frees the dP/dQ columns), then its
-        // 16 vector reductions are issued in groups of 4 between later work so
-        // the load/store queue never fills in one burst
-        uint32_t xq[64];
+        // dQ partial: read out of TMEM (frees the dP/dQ columns), then its 8
+        // vector reductions go out in two groups between later work
+        uint32_t xq[32];
         float *dq_base = nullptr;
         auto read_dq = [&](int it) {
             const int h = kvh * p.G + it / n_m;
             const int m = m_lo + it % n_m;
             tmem_ld32p(tdP + lane_off + c0, xq);
-            tmem_ld32p(tdP + lane_off + c0 + 32, xq + 32);
             tmem_ld_wait();
             tmem_ld_fence32p(xq);
-            tmem_ld_fence32p(xq + 32);
             tc_fence_before();
             mbar_arrive(dq_empty);
             dq_base = (static_cast<int64_t>(m) * kBM + j < p.N)
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 j * 4
                           : nullptr;
         };
-        auto reduce_dq_part = [&](int part) {  // groups 4*part .. 4*part+3
+        auto reduce_dq_part = [&](int part) {  // groups 4*part .. 4*part+3 of 8
             if (dq_base != nullptr) {
 #pragma unroll
                 for (int g = 4 * part; g < 4 * part + 4; ++g)
@@ -422,35 +422,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t u[64];
+            uint32_t u[32];
             tmem_ld32p(tS + lane_off + c0, u);
-            tmem_ld32p(tS + lane_off + c0 + 32, u + 32);
             tmem_ld_wait();
             tmem_ld_fence32p(u);
-            tmem_ld_fence32p(u + 32);
-            const bool full = (q0 + c0 >= lo) && (q0 + c0 + 64 <= hi);
-            uint32_t pk[32];
+            // P^T = 2^(S^T * scale * log2(e) - lse * log2(e)), 0 where masked
+            uint32_t pk[16];
 #pragma unroll
-            for (int c = 0; c < 64; c += 4) {
+            for (int c = 0; c < 32; c += 4) {
                 const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + c);
-                float pv[4];
-                pv[0] = ex2_approx(fmaf(__uint_as_float(u[c + 0]), sl2, -l4.x));
-                pv[1] = ex2_approx(fmaf(__uint_as_float(u[c + 1]), sl2, -l4.y));
-                pv[2] = ex2_approx(fmaf(__uint_as_float(u[c + 2]), sl2, -l4.z));
-                pv[3] = ex2_approx(fmaf(__uint_as_float(u[c + 3]), sl2, -l4.w));
-                if (!full) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int64_t row = q0 + c0 + c + e;
-                        if (row < lo || row >= hi)
-                            pv[e] = 0.f;
-                    }
-                }
-                pk[c / 2] = pack_bf16x2(pv[0], pv[1]);
-                pk[c / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+                const float2 x01 = ffma2(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2,
+                                         make_float2(-l4.x, -l4.y));
+                const float2 x23 = ffma2(make_float2(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])), sl2,
+                                         make_float2(-l4.z, -l4.w));
+                pk[c / 2] = pack_bf16x2(ex2_approx(x01.x), ex2_approx(x01.y));
+                pk[c / 2 + 1] = pack_bf16x2(ex2_approx(x23.x), ex2_approx(x23.y));
             }
-            // P^T of this half into its own S columns (c0 .. c0+31)
-            tmem_st32p(tS + lane_off + c0, pk);
+            if (!((q0 + c0 >= lo) && (q0 + c0 + 32 <= hi))) {
+                // boundary tile for this key: zero the probabilities of rows
+                // outside [lo, hi)
+                const int lo_c = static_cast<int>(max(min(lo - (q0 + c0), int64_t(32)), int64_t(0)));
+                const int hi_c = static_cast<int>(max(min(hi - (q0 + c0), int64_t(32)), int64_t(0)));
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    const uint32_t keep_lo = (c >= lo_c && c < hi_c) ? 0x0000ffffu : 0u;
+                    const uint32_t keep_hi = (c + 1 >= lo_c && c + 1 < hi_c) ? 0xffff0000u : 0u;
+                    pk[c / 2] &= (keep_lo | keep_hi);
+                }
+            }
+            // P^T of these 32 query columns, packed, into S columns c0 .. c0+15
+            tmem_st16p(tS + lane_off + c0, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(p_full);
@@ -473,53 +474,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
+            uint32_t dp[32];
+            tmem_ld32p(tdP + lane_off + c0, dp);
+            tmem_ld_wait();
+            tmem_ld_fence32p(dp);
+            // dS^T = P^T (dP^T - D), packed bf16, into the swizzled row
 #pragma unroll
-            for (int cb = 0; cb < 64; cb += 32) {
-                reduce_dq_part(1 + cb / 32);
-                uint32_t dp[32];
-                tmem_ld32p(tdP + lane_off + c0 + cb, dp);
-                tmem_ld_wait();
-                tmem_ld_fence32p(dp);
-                uint32_t dsp[16];
+            for (int qd = 0; qd < 4; ++qd) {
+                uint32_t dsp[4];
 #pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(D_s + cb + c);
-                    const uint32_t pa = pk[(cb + c) / 2], pb = pk[(cb + c) / 2 + 1];
-                    const float ds0 = bf16lo(pa) * (__uint_as_float(dp[c + 0]) - d4.x);
-                    const float ds1 = bf16hi(pa) * (__uint_as_float(dp[c + 1]) - d4.y);
-                    const float ds2 = bf16lo(pb) * (__uint_as_float(dp[c + 2]) - d4.z);
-                    const float ds3 = bf16hi(pb) * (__uint_as_float(dp[c + 3]) - d4.w);
-                    dsp[c / 2] = pack_bf16x2(ds0, ds1);
-                    dsp[c / 2 + 1] = pack_bf16x2(ds2, ds3);
+                for (int e = 0; e < 4; ++e) {
+                    const int c = qd * 8 + 2 * e;
+                    const float2 d2 = *reinterpret_cast<const float2 *>(D_s + c);
+                    const float2 t = fadd2(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
+                                           make_float2(-d2.x, -d2.y));
+                    const float2 ds = fmul2(make_float2(bf16lo(pk[c / 2]), bf16hi(pk[c / 2])), t);
+                    dsp[e] = pack_bf16x2(ds.x, ds.y);
                 }
-                // columns c0+cb .. +31 = four 16-byte units of this half's swizzled row
-#pragma unroll
-                for (int qd = 0; qd < 4; ++qd) {
-                    const int unit = (cb / 8) + qd;  // 0..7 within the 64-column chunk
-                    const int phys = unit ^ (j & 7);
-                    *reinterpret_cast<uint4 *>(ds_chunk + phys * 16) =
-                        make_uint4(dsp[4 * qd], dsp[4 * qd + 1], dsp[4 * qd + 2], dsp[4 * qd + 3]);
-                }
+                const int unit = (cq & 1) * 4 + qd;  // 16-byte unit within the 64-column chunk
+                *reinterpret_cast<uint4 *>(ds_row + ((unit ^ (j & 7)) * 16)) =
+                    make_uint4(dsp[0], dsp[1], dsp[2], dsp[3]);
             }
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(ds_full);
-            reduce_dq_part(3);
+            reduce_dq_part(1);
         }
         if (ok && n_it > 0) {
             if (mbar_wait_warp(dq_full, (n_it - 1) & 1, p.w, 0x76)) {
                 tc_fence_after();
                 read_dq(n_it - 1);
-#pragma unroll
-                for (int part = 0; part < 4; ++part)
-                    reduce_dq_part(part);
+                reduce_dq_part(0);
+                reduce_dq_part(1);
             } else {
                 ok = false;
             }
         }
         if (!ok)
             *abort_flag = 1;
-        // ---- dK, dV epilogue: key row j, d columns c0 .. c0+63 ----
+        // ---- dK, dV epilogue: key row j, d columns c0 .. c0+31 ----
         if (mbar_wait_warp(dkv_done, 0, p.w, 0x78) && ok) {
             tc_fence_after();
             const bool store = key < p.N;
@@ -529,24 +522,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t src = (which ? tdK : tdV) + lane_off + c0;
                 const float f = which ? p.scale : 1.f;
                 uint16_t *dst = (which ? p.dk : p.dv) + rowoff;
+                uint32_t x[32];
+                tmem_ld32p(src, x);  // warp-collective: all lanes
+                tmem_ld_wait();
+                tmem_ld_fence32p(x);
+                uint32_t o16[16];
 #pragma unroll
-                for (int cb = 0; cb < 64; cb += 32) {
-                    uint32_t x[32];
-                    tmem_ld32p(src + cb, x);  // warp-collective: all lanes
-                    tmem_ld_wait();
-                    tmem_ld_fence32p(x);
-                    uint32_t o16[16];
+                for (int c = 0; c < 16; ++c)
+                    o16[c] = (n_it > 0) ? pack_bf16x2(__uint_as_float(x[2 * c]) * f, __uint_as_float(x[2 * c + 1]) * f)
+                                        : 0u;
+                if (store) {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        o16[c] = (n_it > 0) ? pack_bf16x2(__uint_as_float(x[2 * c]) * f,
-                                                          __uint_as_float(x[2 * c + 1]) * f)
-                                            : 0u;
-                    if (store) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            reinterpret_cast<uint4 *>(dst + cb)[c] =
-                                make_uint4(o16[4 * c], o16[4 * c + 1], o16[4 * c + 2], o16[4 * c + 3]);
-                    }
+                    for (int c = 0; c < 4; ++c)
+                        reinterpret_cast<uint4 *>(dst)[c] =
+                            make_uint4(o16[4 * c], o16[4 * c + 1], o16[4 * c + 2], o16[4 * c + 3]);
                 }
             }
         }
@@ -556,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 9)
+    if (warp == kMmaWarp)
         tmem_dealloc(tbase, 512);
 }
 
