@@ -219,9 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProdWarp && lane == 0) {
         for (int i = 0; i < 14; ++i)
             mbar_init(&bars[i], 1);
-        mbar_init(ds_full, kCompWarps * 32);  // every compute thread
-        mbar_init(p_full, kCompWarps * 32);
-        mbar_init(dq_empty, kCompWarps * 32);
+        mbar_init(ds_full, kCompWarps);  // one elected arrival per compute warp
+        mbar_init(p_full, kCompWarps);
+        mbar_init(dq_empty, kCompWarps);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -347,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss(tdK, desc_sw128(sdS + off, 16, 1024), desc_sw128(sQ + kk * 2048, kChunk, 1024), id_kmn,
                            (it > 0 || kk > 0) ? 1u : 0u);
                 }
+                mma_commit(&q_empty[slot]);  // dK was the last reader of Q, lse, D and dO of this slot
                 // dQ = dS K      (A = dS, query index contiguous; B = K, d contiguous)
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
@@ -354,7 +355,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                            id_mnmn, kk > 0);
                 mma_commit(dq_full);
                 mma_commit(ds_empty);
-                mma_commit(&q_empty[slot]);
             }
             if (!ok)
                 *abort_flag = 1;
@@ -395,7 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             tmem_ld_fence32p(xq);
             tc_fence_before();
-            mbar_arrive(dq_empty);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(dq_empty);
             dq_base = (static_cast<int64_t>(m) * kBM + j < p.N)
                           ? p.dq_acc +
                                 (((static_cast<int64_t>(sb) * p.Hq + h) * (p.Npad / kBM) + m) * 32 + c0 / 4) *
@@ -454,7 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st16p(tS + lane_off + c0, pk);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(p_full);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(p_full);
             // the previous iteration's dQ partial (frees the dP/dQ columns)
             if (it > 0) {
                 if (!mbar_wait_warp(dq_full, (it - 1) & 1, p.w, 0x73)) {
@@ -497,7 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(ds_full);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(ds_full);
             reduce_dq_part(1);
         }
         if (ok && n_it > 0) {

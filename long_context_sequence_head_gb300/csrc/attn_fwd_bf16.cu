@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], kBM);
+            mbar_init(&p_full[i], 4);  // one elected arrival per softmax warp
         }
         mbar_init(o_done, 1);
         mbar_init(drain, 1);
@@ -358,7 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&p_full[t]);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&p_full[t]);
             }
             if (!ok)
                 *abort_flag = 1;
