@@ -223,6 +223,29 @@ def run_ours(args, rank, world, dist):
     ph = [statistics.mean(p[j] for p in phase) for j in range(5)]
     elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
 
+    # ---- the same step through the fused seq-layout calls (no swaps)
+    fused = None
+    if full and (N // P) % 128 == 0:
+        def fused_step():
+            uly.ulysses_attn_fwd_seq(q, k, v, o_seq, lse, P, causal=w.causal, cu_seqlens=cu, workspace=ws_f)
+            uly.ulysses_attn_bwd_seq(q, k, v, o_seq, lse, do, dq_seq, dk_seq, dv_seq, P, causal=w.causal,
+                                     cu_seqlens=cu, workspace=ws_b)
+        for _ in range(2):
+            fused_step()
+        barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            fused_step()
+        f1.record(stream)
+        barrier()
+        fused_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, dist, dev)
+        fused = {"ms_per_step": fused_ms, "launches_per_step": 1 + 3}
+        st, site = uly.ulysses_get_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} at site {site:#x} in the fused timing")
+
     # ---- end to end: host buffers in pinned memory, copies inside the timed region
     pin = lambda x: torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     h_in = {n: pin(x).copy_(x) for n, x in (("q", q), ("k", k), ("v", v), ("dout", do))}
@@ -298,6 +321,11 @@ def run_ours(args, rank, world, dist):
                      else "fallback 1.7 PFLOP/s sustained"},
         "e2e": {"value": round(whole_job_throughput(world, step_flops, e2e_ms), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "fused_seq_layout_path": None if fused is None else {
+            "what": "ulysses_attn_fwd_seq + ulysses_attn_bwd_seq: same step without the swap kernels",
+            "ms_per_step": round(fused["ms_per_step"], 3),
+            "value": round(whole_job_throughput(world, step_flops, fused["ms_per_step"]), 2), "unit": UNIT,
+            "tokens_per_s": round(world * B * N / (fused["ms_per_step"] * 1e-3), 1)},
         "clocks": clk.summary(),
         "gpu_launches": args.steps * ((8 if full else 4) + 1 + 3),
     }

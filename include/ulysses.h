@@ -152,6 +152,43 @@ uly_status ulysses_attn_bwd(const void *q, const void *k, const void *v, const v
                             size_t workspace_bytes, void *stream);
 
 /*
+ * The swap -> attention -> swap pipeline without the swaps: attention over all
+ * P head shards read straight from the sequence-sharded buffers, outputs
+ * written straight back to them.  Same results as
+ *   ulysses_seq_to_head(q/k/v) ; ulysses_attn_fwd(num_shards = P) ;
+ *   ulysses_head_to_seq(o)
+ * because on one device head shard r is just a strided view of the seq
+ * buffer (the all-to-all moves data between GPUs; on one GPU it only
+ * relabels rows).  Source: as ulysses_seq_to_head and ulysses_attn_fwd.
+ *
+ * q_seq, o_seq : device, [P][B][N/P][Hq][d]     k_seq, v_seq : [P][B][N/P][Hkv][d]
+ * lse          : device fp32, [P][B][Hq/P][N]   (head shard r, local head h)
+ * Hq, Hkv are the GLOBAL head counts; H % P == 0 for both (ULY_ERR_INVALID_ARG).
+ * bf16 also needs (N/P) % 128 == 0 so that no 128-token tile straddles two
+ * sequence shards (ULY_ERR_UNSUPPORTED otherwise).  workspace: as
+ * ulysses_attn_workspace_size(B, N, Hq/P, Hkv/P, d, P, num_docs, 0, dtype).
+ * Other arguments, validation and errors as ulysses_attn_fwd.
+ */
+uly_status ulysses_attn_fwd_seq(const void *q_seq, const void *k_seq, const void *v_seq, void *o_seq,
+                                float *lse, int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_t d,
+                                int32_t P, int32_t causal, const int32_t *cu_seqlens_host,
+                                int32_t num_docs, float softmax_scale, uly_dtype dtype, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/*
+ * Backward of ulysses_attn_fwd_seq: dout_seq in, dq_seq / dk_seq / dv_seq out,
+ * all in the sequence-sharded layout (the backward of the swaps is the
+ * inverse swap, so no swap is needed here either).  workspace: as
+ * ulysses_attn_workspace_size(B, N, Hq/P, Hkv/P, d, P, num_docs, 1, dtype).
+ */
+uly_status ulysses_attn_bwd_seq(const void *q_seq, const void *k_seq, const void *v_seq,
+                                const void *o_seq, const float *lse, const void *dout_seq,
+                                void *dq_seq, void *dk_seq, void *dv_seq, int64_t B, int64_t N,
+                                int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int32_t causal,
+                                const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale,
+                                uly_dtype dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * ulysses_attn_bwd without a workspace, for callers that cannot allocate
  * device memory: code running inside an allocator's own hooks, a process
  * whose device memory pool is fixed up front, a plugin that is handed only

@@ -32,7 +32,8 @@ _STATUS = {0: "ULY_OK", 1: "ULY_ERR_INVALID_ARG", 2: "ULY_ERR_UNSUPPORTED", 3: "
 
 # every symbol include/ulysses.h declares
 EXPORTED = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_workspace_size",
-            "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc", "ulysses_get_device_status",
+            "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_attn_fwd_seq", "ulysses_attn_bwd_seq",
+            "ulysses_attn_bwd_noalloc", "ulysses_get_device_status",
             "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout",
             "ulysses_status_string", "ulysses_version")
 
@@ -70,6 +71,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.ulysses_attn_workspace_size.restype = sz
     lib.ulysses_attn_fwd.argtypes = [vp] * 5 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp, sz, vp]
     lib.ulysses_attn_bwd.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp, sz, vp]
+    lib.ulysses_attn_fwd_seq.argtypes = lib.ulysses_attn_fwd.argtypes
+    lib.ulysses_attn_bwd_seq.argtypes = lib.ulysses_attn_bwd.argtypes
     lib.ulysses_attn_bwd_noalloc.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp]
     lib.ulysses_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.ulysses_set_wait_limit_ns.argtypes = [u64]
@@ -78,7 +81,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.ulysses_status_string.restype = ctypes.c_char_p
     lib.ulysses_version.restype = i32
     for name in ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_fwd", "ulysses_attn_bwd",
-                 "ulysses_attn_bwd_noalloc",
+                 "ulysses_attn_bwd_noalloc", "ulysses_attn_fwd_seq", "ulysses_attn_bwd_seq",
                  "ulysses_get_device_status", "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout"):
         getattr(lib, name).restype = i32
     _lib = lib
@@ -193,6 +196,44 @@ def ulysses_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = True,
         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, N, Hq, Hkv, d, S, int(bool(causal)), cu_p, nd,
         float(softmax_scale), _dt(q), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
     return dq, dk, dv
+
+
+def ulysses_attn_fwd_seq(q_seq, k_seq, v_seq, o_seq, lse, P: int, causal: bool = True,
+                         cu_seqlens: Optional[Sequence[int]] = None, softmax_scale: float = 0.0,
+                         workspace: Optional[torch.Tensor] = None, stream=None):
+    """Attention over all P head shards read from and written to the
+    sequence-sharded layout [P][B][N/P][H][d] (no swaps); lse [P][B][Hq/P][N]."""
+    _dev(q_seq, k_seq, v_seq, o_seq, lse)
+    Ps, B, Np, Hq, d = q_seq.shape
+    Hkv = k_seq.shape[3]
+    N = Np * P
+    cu_p, nd, _keep = _cu(cu_seqlens)
+    need = ulysses_attn_workspace_size(B, N, Hq // P, Hkv // P, d, P, nd, False, q_seq.dtype)
+    ws = _workspace(workspace, need, q_seq.device)
+    _check("ulysses_attn_fwd_seq", load().ulysses_attn_fwd_seq(
+        q_seq.data_ptr(), k_seq.data_ptr(), v_seq.data_ptr(), o_seq.data_ptr(), lse.data_ptr(), B, N, Hq, Hkv,
+        d, P, int(bool(causal)), cu_p, nd, float(softmax_scale), _dt(q_seq), ws.data_ptr(),
+        ws.numel() * ws.element_size(), _stream(stream)))
+    return o_seq, lse
+
+
+def ulysses_attn_bwd_seq(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_seq, dv_seq, P: int,
+                         causal: bool = True, cu_seqlens: Optional[Sequence[int]] = None,
+                         softmax_scale: float = 0.0, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Backward of ulysses_attn_fwd_seq, all tensors in the sequence-sharded layout."""
+    _dev(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_seq, dv_seq)
+    Ps, B, Np, Hq, d = q_seq.shape
+    Hkv = k_seq.shape[3]
+    N = Np * P
+    cu_p, nd, _keep = _cu(cu_seqlens)
+    need = ulysses_attn_workspace_size(B, N, Hq // P, Hkv // P, d, P, nd, True, q_seq.dtype)
+    ws = _workspace(workspace, need, q_seq.device)
+    _check("ulysses_attn_bwd_seq", load().ulysses_attn_bwd_seq(
+        q_seq.data_ptr(), k_seq.data_ptr(), v_seq.data_ptr(), o_seq.data_ptr(), lse.data_ptr(),
+        dout_seq.data_ptr(), dq_seq.data_ptr(), dk_seq.data_ptr(), dv_seq.data_ptr(), B, N, Hq, Hkv, d, P,
+        int(bool(causal)), cu_p, nd, float(softmax_scale), _dt(q_seq), ws.data_ptr(),
+        ws.numel() * ws.element_size(), _stream(stream)))
+    return dq_seq, dk_seq, dv_seq
 
 
 def ulysses_attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = True,

@@ -68,8 +68,9 @@ struct BwdParams {
     const float *lse2;  // [SB][Hq][Npad]
     const float *Dv;    // [SB][Hq][Npad]
     float *dq_acc;      // [SB][Hq][Npad/128][32][128][4]
-    uint16_t *dk, *dv;  // [SB][N][Hkv][128]
+    uint16_t *dk, *dv;  // rows like k, v
     WaitCfg w;
+    RowLayout L;
 };
 
 __device__ __forceinline__ void doc_range(const BwdParams &p, int64_t i, int64_t &lo, int64_t &hi)
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *__restrict
                                                       const uint16_t *__restrict__ dout,
                                                       const float *__restrict__ lse, float *__restrict__ lse2,
                                                       float *__restrict__ Dv, int64_t SB, int64_t N, int64_t Npad,
-                                                      int Hq)
+                                                      int Hq, RowLayout L)
 {
     // one warp per (sb, h, row); lane reads 4 bf16 of O and dO (8 bytes each)
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *__restrict
         }
         return;
     }
-    const int64_t off = ((sb * N + i) * Hq + h) * kD + lane * 4;
+    const int64_t off = L.off(N, sb, i, Hq, h, kD) + lane * 4;
     const uint2 a = *reinterpret_cast<const uint2 *>(o + off);
     const uint2 b = *reinterpret_cast<const uint2 *>(dout + off);
     float acc = bf16lo(a.x) * bf16lo(b.x);
@@ -141,7 +142,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *__restrict
 
 // ---------------------------------------------------------- dq convert
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc, uint16_t *__restrict__ dq,
-                                                         int64_t SB, int64_t N, int64_t Npad, int Hq, float scale)
+                                                         int64_t SB, int64_t N, int64_t Npad, int Hq, float scale,
+                                                         RowLayout L)
 {
     // thread -> (sb, h, row, group of 4 columns); lanes vary the group so the
     // bf16 row writes are contiguous
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
     uint2 out;
     out.x = pack_bf16x2(v.x * scale, v.y * scale);
     out.y = pack_bf16x2(v.z * scale, v.w * scale);
-    *reinterpret_cast<uint2 *>(dq + ((sb * N + i) * Hq + h) * kD + g * 4) = out;
+    *reinterpret_cast<uint2 *>(dq + L.off(N, sb, i, Hq, h, kD) + g * 4) = out;
 }
 
 // ----------------------------------------------------------------- main
@@ -243,10 +245,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
             mbar_expect_tx(kv_full, 2 * kTile);
-            tma_load_4d(smem + BwdSmem::kK, &tm_k, kv_full, 0, kvh, static_cast<int>(kv0), sb);
-            tma_load_4d(smem + BwdSmem::kK + kChunk, &tm_k, kv_full, 64, kvh, static_cast<int>(kv0), sb);
-            tma_load_4d(smem + BwdSmem::kV, &tm_v, kv_full, 0, kvh, static_cast<int>(kv0), sb);
-            tma_load_4d(smem + BwdSmem::kV + kChunk, &tm_v, kv_full, 64, kvh, static_cast<int>(kv0), sb);
+            int c1, c2, c3, c4;
+            p.L.tile(sb, kv0, p.Hkv, kvh, c1, c2, c3, c4);
+            tma_load_5d(smem + BwdSmem::kK, &tm_k, kv_full, 0, c1, c2, c3, c4);
+            tma_load_5d(smem + BwdSmem::kK + kChunk, &tm_k, kv_full, 64, c1, c2, c3, c4);
+            tma_load_5d(smem + BwdSmem::kV, &tm_v, kv_full, 0, c1, c2, c3, c4);
+            tma_load_5d(smem + BwdSmem::kV + kChunk, &tm_v, kv_full, 64, c1, c2, c3, c4);
             int issued = 0;
             for (int it = 0; it < n_it && !*abort_flag; ++it) {
                 const int slot = it & 1;
@@ -259,10 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_expect_tx(&q_full[slot], 2 * kTile + 2 * 512);
                 uint8_t *sq = smem + BwdSmem::kQ + slot * kTile;
                 uint8_t *sdo = smem + BwdSmem::kdO + slot * kTile;
-                tma_load_4d(sq, &tm_q, &q_full[slot], 0, h, m * kBM, sb);
-                tma_load_4d(sq + kChunk, &tm_q, &q_full[slot], 64, h, m * kBM, sb);
-                tma_load_4d(sdo, &tm_do, &q_full[slot], 0, h, m * kBM, sb);
-                tma_load_4d(sdo + kChunk, &tm_do, &q_full[slot], 64, h, m * kBM, sb);
+                p.L.tile(sb, static_cast<int64_t>(m) * kBM, p.Hq, h, c1, c2, c3, c4);
+                tma_load_5d(sq, &tm_q, &q_full[slot], 0, c1, c2, c3, c4);
+                tma_load_5d(sq + kChunk, &tm_q, &q_full[slot], 64, c1, c2, c3, c4);
+                tma_load_5d(sdo, &tm_do, &q_full[slot], 0, c1, c2, c3, c4);
+                tma_load_5d(sdo + kChunk, &tm_do, &q_full[slot], 64, c1, c2, c3, c4);
                 const int64_t roff = (static_cast<int64_t>(sb) * p.Hq + h) * p.Npad + static_cast<int64_t>(m) * kBM;
                 bulk_g2s(smem + BwdSmem::kLse + slot * 512, p.lse2 + roff, 512, &q_full[slot]);
                 bulk_g2s(smem + BwdSmem::kDv + slot * 512, p.Dv + roff, 512, &q_full[slot]);
@@ -522,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mbar_wait_warp(dkv_done, 0, p.w, 0x78) && ok) {
             tc_fence_after();
             const bool store = key < p.N;
-            const int64_t rowoff = ((static_cast<int64_t>(sb) * p.N + (store ? key : 0)) * p.Hkv + kvh) * kD + c0;
+            const int64_t rowoff = p.L.off(p.N, sb, store ? key : 0, p.Hkv, kvh, kD) + c0;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 const uint32_t src = (which ? tdK : tdV) + lane_off + c0;
@@ -555,19 +560,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tbase, 512);
 }
 
-CUresult make_map(CUtensorMap *map, const void *base, int64_t SB, int64_t N, int H)
-{
-    cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
-                          static_cast<cuuint64_t>(SB)};
-    cuuint64_t strides[3] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(H) * kD * 2,
-                             static_cast<cuuint64_t>(N) * H * kD * 2};
-    cuuint32_t box[4] = {64, 1, 128, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    return tensor_map_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-}
-
 }  // namespace
 
 cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
@@ -577,8 +569,8 @@ cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *
     if (s.d != kD)
         return cudaErrorInvalidValue;
     CUtensorMap tq, tk, tv, tdo;
-    if (make_map(&tq, q, s.SB, s.N, s.Hq) != CUDA_SUCCESS || make_map(&tk, k, s.SB, s.N, s.Hkv) != CUDA_SUCCESS ||
-        make_map(&tv, v, s.SB, s.N, s.Hkv) != CUDA_SUCCESS || make_map(&tdo, dout, s.SB, s.N, s.Hq) != CUDA_SUCCESS)
+    if (make_rows_map_bf16(&tq, q, s, s.Hq) != CUDA_SUCCESS || make_rows_map_bf16(&tk, k, s, s.Hkv) != CUDA_SUCCESS ||
+        make_rows_map_bf16(&tv, v, s, s.Hkv) != CUDA_SUCCESS || make_rows_map_bf16(&tdo, dout, s, s.Hq) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const int64_t Npad = scr.Npad;
     cudaError_t e;
@@ -588,7 +580,7 @@ cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *
         const int64_t blocks = (warps * 32 + 255) / 256;
         bwd_pre_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
             static_cast<const uint16_t *>(o), static_cast<const uint16_t *>(dout), lse, scr.lse2, scr.D, s.SB, s.N,
-            Npad, s.Hq);
+            Npad, s.Hq, s.L);
         e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;
@@ -616,6 +608,7 @@ cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *
     p.dk = static_cast<uint16_t *>(dk);
     p.dv = static_cast<uint16_t *>(dv);
     p.w = wait_cfg();
+    p.L = s.L;
     const size_t smem = BwdSmem::kTotal;
     e = cudaFuncSetAttribute(attn_bwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
@@ -630,7 +623,7 @@ cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *
     {
         const int64_t total = s.SB * s.Hq * s.N * 32;
         dq_convert_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
-            scr.dq_acc, static_cast<uint16_t *>(dq), s.SB, s.N, Npad, s.Hq, s.scale);
+            scr.dq_acc, static_cast<uint16_t *>(dq), s.SB, s.N, Npad, s.Hq, s.scale, s.L);
     }
     return cudaGetLastError();
 }

@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(AttnShape s, const
     if (i >= s.N)
         return;
     const int kvh = h / (s.Hq / s.Hkv);
-    const float *qi = q + ((sb * s.N + i) * s.Hq + h) * D;
+    const float *qi = q + s.L.off(s.N, sb, i, s.Hq, h, D);
     float qr[E], acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -72,8 +72,8 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(AttnShape s, const
         hi = i + 1;
     float m = -INFINITY, l = 0.f;
     for (int64_t j = lo; j < hi; ++j) {
-        const float *kj = k + ((sb * s.N + j) * s.Hkv + kvh) * D;
-        const float *vj = v + ((sb * s.N + j) * s.Hkv + kvh) * D;
+        const float *kj = k + s.L.off(s.N, sb, j, s.Hkv, kvh, D);
+        const float *vj = v + s.L.off(s.N, sb, j, s.Hkv, kvh, D);
         float part = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e)
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(AttnShape s, const
             acc[e] = fmaf(p, vj[lane + 32 * e], acc[e] * alpha);
         m = m_new;
     }
-    float *oi = o + ((sb * s.N + i) * s.Hq + h) * D;
+    float *oi = o + s.L.off(s.N, sb, i, s.Hq, h, D);
     const float inv = 1.f / l;
 #pragma unroll
     for (int e = 0; e < E; ++e)
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_pre_f32_kernel(AttnShape s, c
     const int64_t sb = blockIdx.z;
     if (i >= s.N)
         return;
-    const int64_t off = ((sb * s.N + i) * s.Hq + h) * D;
+    const int64_t off = s.L.off(s.N, sb, i, s.Hq, h, D);
     float part = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e)
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_f32_kernel(AttnShape s, co
     if (i >= s.N)
         return;
     const int kvh = h / (s.Hq / s.Hkv);
-    const int64_t off = ((sb * s.N + i) * s.Hq + h) * D;
+    const int64_t off = s.L.off(s.N, sb, i, s.Hq, h, D);
     float qr[E], dor[E], acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -152,8 +152,8 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_f32_kernel(AttnShape s, co
     if (s.causal)
         hi = i + 1;
     for (int64_t j = lo; j < hi; ++j) {
-        const float *kj = k + ((sb * s.N + j) * s.Hkv + kvh) * D;
-        const float *vj = v + ((sb * s.N + j) * s.Hkv + kvh) * D;
+        const float *kj = k + s.L.off(s.N, sb, j, s.Hkv, kvh, D);
+        const float *vj = v + s.L.off(s.N, sb, j, s.Hkv, kvh, D);
         float ps = 0.f, pd = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkv_f32_kernel(AttnShape s, c
     if (j >= s.N)
         return;
     const int G = s.Hq / s.Hkv;
-    const int64_t off = ((sb * s.N + j) * s.Hkv + kvh) * D;
+    const int64_t off = s.L.off(s.N, sb, j, s.Hkv, kvh, D);
     float kr[E], vr[E], ak[E], av[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkv_f32_kernel(AttnShape s, c
         lo = j;  // rows i >= j attend to key j
     for (int h = kvh * G; h < (kvh + 1) * G; ++h) {
         for (int64_t i = lo; i < hi; ++i) {
-            const int64_t qo = ((sb * s.N + i) * s.Hq + h) * D;
+            const int64_t qo = s.L.off(s.N, sb, i, s.Hq, h, D);
             float ps = 0.f, pd = 0.f;
 #pragma unroll
             for (int e = 0; e < E; ++e) {

@@ -52,6 +52,7 @@ struct FwdParams {
     uint16_t *o;
     float *lse;
     WaitCfg w;
+    RowLayout L;
 };
 
 __device__ __forceinline__ void doc_range(const FwdParams &p, int64_t i, int64_t &lo, int64_t &hi)
@@ -144,11 +145,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             mbar_expect_tx(q_full, has1 ? 2 * kTileBytes : kTileBytes);
-            tma_load_4d(smem + FwdSmem::kQ0, &tm_q, q_full, 0, h0, static_cast<int>(q0), sb);
-            tma_load_4d(smem + FwdSmem::kQ0 + kChunk, &tm_q, q_full, 64, h0, static_cast<int>(q0), sb);
+            int c1, c2, c3, c4;
+            p.L.tile(sb, q0, p.Hq, h0, c1, c2, c3, c4);
+            tma_load_5d(smem + FwdSmem::kQ0, &tm_q, q_full, 0, c1, c2, c3, c4);
+            tma_load_5d(smem + FwdSmem::kQ0 + kChunk, &tm_q, q_full, 64, c1, c2, c3, c4);
             if (has1) {
-                tma_load_4d(smem + FwdSmem::kQ1, &tm_q, q_full, 0, h0 + 1, static_cast<int>(q0), sb);
-                tma_load_4d(smem + FwdSmem::kQ1 + kChunk, &tm_q, q_full, 64, h0 + 1, static_cast<int>(q0), sb);
+                p.L.tile(sb, q0, p.Hq, h0 + 1, c1, c2, c3, c4);
+                tma_load_5d(smem + FwdSmem::kQ1, &tm_q, q_full, 0, c1, c2, c3, c4);
+                tma_load_5d(smem + FwdSmem::kQ1 + kChunk, &tm_q, q_full, 64, c1, c2, c3, c4);
             }
             int issued = 0;
             for (int j = 0; j < n_kv && !*abort_flag; ++j) {
@@ -164,8 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *dst = smem + FwdSmem::kSlot0 + slot * kTileBytes;
                     const CUtensorMap *tm = which ? &tm_v : &tm_k;
                     mbar_expect_tx(&kv_full[slot], kTileBytes);
-                    tma_load_4d(dst, tm, &kv_full[slot], 0, kvh, key0, sb);
-                    tma_load_4d(dst + kChunk, tm, &kv_full[slot], 64, kvh, key0, sb);
+                    p.L.tile(sb, key0, p.Hkv, kvh, c1, c2, c3, c4);
+                    tma_load_5d(dst, tm, &kv_full[slot], 0, c1, c2, c3, c4);
+                    tma_load_5d(dst + kChunk, tm, &kv_full[slot], 64, c1, c2, c3, c4);
                     ++issued;
                 }
                 if (!ok) {
@@ -380,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                      __uint_as_float(o32[2 * c + 1]) * inv);
                 }
                 if (row < p.N) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((sb * p.N + row) * p.Hq + h) * kD);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + p.L.off(p.N, sb, row, p.Hq, h, kD));
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
                         dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
@@ -399,25 +404,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tbase, 512);
 }
 
-CUresult make_head_map(CUtensorMap *map, const void *base, int64_t SB, int64_t N, int H)
-{
-    // head layout [SB][N][H][128] bf16 as a 4-D map {128, H, N, SB}; box {64, 1, 128, 1}
-    cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
-                          static_cast<cuuint64_t>(SB)};
-    cuuint64_t strides[3] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(H) * kD * 2,
-                             static_cast<cuuint64_t>(N) * H * kD * 2};
-    cuuint32_t box[4] = {64, 1, kBM, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    return tensor_map_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-}
-
 }  // namespace
 
-CUresult make_head_map_bf16(CUtensorMap *map, const void *base, int64_t SB, int64_t N, int H)
+CUresult make_rows_map_bf16(CUtensorMap *map, const void *base, const AttnShape &s, int H)
 {
-    return make_head_map(map, base, SB, N, H);
+    // head layout: [S][B][N][H][d]; seq layout: [P][B][N/P][P*H][d]
+    const int64_t B = s.L.B;
+    const int64_t outer = s.L.seq ? s.L.P : s.SB / B;
+    const int64_t T = s.L.seq ? s.L.Np : s.N;
+    const int64_t Hd = s.L.seq ? static_cast<int64_t>(H) * s.L.P : H;
+    cuuint64_t dims[5] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(Hd), static_cast<cuuint64_t>(T),
+                          static_cast<cuuint64_t>(B), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[4] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(Hd) * kD * 2,
+                             static_cast<cuuint64_t>(T) * Hd * kD * 2, static_cast<cuuint64_t>(B) * T * Hd * kD * 2};
+    cuuint32_t box[5] = {64, 1, kBM, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return tensor_map_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 cudaError_t launch_attn_fwd_bf16(const AttnShape &s, const void *q, const void *k, const void *v, void *o,
@@ -426,9 +430,8 @@ cudaError_t launch_attn_fwd_bf16(const AttnShape &s, const void *q, const void *
     if (s.d != kD)
         return cudaErrorInvalidValue;
     CUtensorMap tq, tk, tv;
-    if (make_head_map(&tq, q, s.SB, s.N, s.Hq) != CUDA_SUCCESS ||
-        make_head_map(&tk, k, s.SB, s.N, s.Hkv) != CUDA_SUCCESS ||
-        make_head_map(&tv, v, s.SB, s.N, s.Hkv) != CUDA_SUCCESS)
+    if (make_rows_map_bf16(&tq, q, s, s.Hq) != CUDA_SUCCESS || make_rows_map_bf16(&tk, k, s, s.Hkv) != CUDA_SUCCESS ||
+        make_rows_map_bf16(&tv, v, s, s.Hkv) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     FwdParams p;
     p.SB = s.SB;
@@ -445,6 +448,7 @@ cudaError_t launch_attn_fwd_bf16(const AttnShape &s, const void *q, const void *
     p.o = static_cast<uint16_t *>(o);
     p.lse = lse;
     p.w = wait_cfg();
+    p.L = s.L;
     const int64_t units = p.SB * p.Hkv * p.npairs * p.n_qtiles;
     const size_t smem = FwdSmem::kTotal + 1024;
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -26,6 +26,44 @@ cudaError_t launch_swap(bool to_head, const void *src, void *dst, int64_t B, int
                         int esize, cudaStream_t stream);
 
 // ----------------------------------------------------------- attention
+// Where the rows of an attention tensor live.
+//   head layout (seq == 0): [S][B][N][H][d], shard-major, what the swap writes;
+//   seq layout  (seq == 1): [P][B][N/P][P*H][d], the sequence-sharded buffer
+//     before the swap: head shard r of local head h is global head r*H + h,
+//     token n sits in sequence shard n / (N/P) at position n % (N/P).
+// Row (sb, n, h) with sb = shard*B + batch.
+struct RowLayout {
+    int seq;
+    int B;
+    int64_t Np;  // N / P (seq layout)
+    int P;       // head shards == sequence shards (seq layout)
+
+    __host__ __device__ int64_t off(int64_t N, int64_t sb, int64_t n, int H, int h, int d) const
+    {
+        if (!seq)
+            return ((sb * N + n) * H + h) * static_cast<int64_t>(d);
+        const int64_t r = sb / B, b = sb % B, s = n / Np, t = n % Np;
+        return (((s * B + b) * Np + t) * (static_cast<int64_t>(H) * P) + r * H + h) * static_cast<int64_t>(d);
+    }
+    // coordinates {head, token, batch, outer} of the 5-D tensor map of this
+    // layout for a tile of rows starting at token n0 (which never straddles a
+    // sequence shard in the seq layout)
+    __host__ __device__ void tile(int64_t sb, int64_t n0, int H, int h, int &c1, int &c2, int &c3, int &c4) const
+    {
+        const int r = static_cast<int>(sb / B), b = static_cast<int>(sb % B);
+        c3 = b;
+        if (!seq) {
+            c1 = h;
+            c2 = static_cast<int>(n0);
+            c4 = r;
+        } else {
+            c1 = r * H + h;
+            c2 = static_cast<int>(n0 % Np);
+            c4 = static_cast<int>(n0 / Np);
+        }
+    }
+};
+
 struct AttnShape {
     int64_t SB;      // num_shards * B (independent (shard, batch) problems)
     int64_t N;       // tokens
@@ -34,7 +72,12 @@ struct AttnShape {
     const int32_t *cu_dev;  // device cu_seqlens [num_docs+1] or nullptr
     int num_docs;
     float scale;      // softmax scale
+    RowLayout L;     // where q/k/v/o/dout/dq/dk/dv rows live
 };
+
+// 5-D bf16 tensor map {d, H, T, B, outer} over a row-major
+// [outer][B][T][H][d] buffer, box {64, 1, 128, 1, 1}, 128-byte swizzle.
+CUresult make_rows_map_bf16(CUtensorMap *map, const void *base, const AttnShape &s, int H);
 
 cudaError_t launch_attn_fwd_f32(const AttnShape &s, const float *q, const float *k, const float *v, float *o,
                                 float *lse, cudaStream_t stream);

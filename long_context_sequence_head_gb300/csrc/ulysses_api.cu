@@ -242,10 +242,14 @@ size_t ulysses_attn_workspace_size(int64_t B, int64_t N, int32_t Hq_local, int32
     return ws_layout(B, N, Hq_local, d, num_shards, num_docs, for_bwd != 0, dtype).total;
 }
 
-uly_status ulysses_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B, int64_t N,
-                            int32_t Hq_local, int32_t Hkv_local, int32_t d, int32_t num_shards, int32_t causal,
-                            const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale, uly_dtype dtype,
-                            void *workspace, size_t workspace_bytes, void *stream)
+}  // extern "C"
+
+namespace {
+
+uly_status attn_fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B, int64_t N,
+                         int32_t Hq_local, int32_t Hkv_local, int32_t d, int32_t num_shards, int32_t causal,
+                         const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale, uly_dtype dtype,
+                         void *workspace, size_t workspace_bytes, void *stream, uly::RowLayout L)
 {
     if (!q || !k || !v || !o || !lse || !workspace)
         return ULY_ERR_INVALID_ARG;
@@ -256,8 +260,8 @@ uly_status ulysses_attn_fwd(const void *q, const void *k, const void *v, void *o
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
         !aligned16(workspace))
         return ULY_ERR_MISALIGNED;
-    const WsLayout L = ws_layout(B, N, Hq_local, d, num_shards, num_docs, false, dtype);
-    if (workspace_bytes < L.total)
+    const WsLayout W = ws_layout(B, N, Hq_local, d, num_shards, num_docs, false, dtype);
+    if (workspace_bytes < W.total)
         return ULY_ERR_WORKSPACE;
     if (uly::tensor_map_encoder() == nullptr || uly::device_status_ptr() == nullptr)
         return ULY_ERR_CUDA;
@@ -272,9 +276,10 @@ uly_status ulysses_attn_fwd(const void *q, const void *k, const void *v, void *o
     sh.num_docs = cu_seqlens_host ? num_docs : 0;
     sh.cu_dev = nullptr;
     sh.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
+    sh.L = L;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     if (cu_seqlens_host) {
-        int32_t *cu_dev = reinterpret_cast<int32_t *>(ws + L.cu_off);
+        int32_t *cu_dev = reinterpret_cast<int32_t *>(ws + W.cu_off);
         cudaError_t e = cudaMemcpyAsync(cu_dev, cu_seqlens_host, sizeof(int32_t) * (num_docs + 1),
                                         cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess)
@@ -287,11 +292,11 @@ uly_status ulysses_attn_fwd(const void *q, const void *k, const void *v, void *o
     return from_cuda(uly::launch_attn_fwd_bf16(sh, q, k, v, o, lse, s));
 }
 
-uly_status ulysses_attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                            const void *dout, void *dq, void *dk, void *dv, int64_t B, int64_t N, int32_t Hq_local,
-                            int32_t Hkv_local, int32_t d, int32_t num_shards, int32_t causal,
-                            const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale, uly_dtype dtype,
-                            void *workspace, size_t workspace_bytes, void *stream)
+uly_status attn_bwd_impl(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                         const void *dout, void *dq, void *dk, void *dv, int64_t B, int64_t N, int32_t Hq_local,
+                         int32_t Hkv_local, int32_t d, int32_t num_shards, int32_t causal,
+                         const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale, uly_dtype dtype,
+                         void *workspace, size_t workspace_bytes, void *stream, uly::RowLayout L)
 {
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
         return ULY_ERR_INVALID_ARG;
@@ -302,8 +307,8 @@ uly_status ulysses_attn_bwd(const void *q, const void *k, const void *v, const v
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
         !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
         return ULY_ERR_MISALIGNED;
-    const WsLayout L = ws_layout(B, N, Hq_local, d, num_shards, num_docs, true, dtype);
-    if (workspace_bytes < L.total)
+    const WsLayout W = ws_layout(B, N, Hq_local, d, num_shards, num_docs, true, dtype);
+    if (workspace_bytes < W.total)
         return ULY_ERR_WORKSPACE;
     if (uly::tensor_map_encoder() == nullptr || uly::device_status_ptr() == nullptr)
         return ULY_ERR_CUDA;
@@ -318,9 +323,10 @@ uly_status ulysses_attn_bwd(const void *q, const void *k, const void *v, const v
     sh.num_docs = cu_seqlens_host ? num_docs : 0;
     sh.cu_dev = nullptr;
     sh.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
+    sh.L = L;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     if (cu_seqlens_host) {
-        int32_t *cu_dev = reinterpret_cast<int32_t *>(ws + L.cu_off);
+        int32_t *cu_dev = reinterpret_cast<int32_t *>(ws + W.cu_off);
         cudaError_t e = cudaMemcpyAsync(cu_dev, cu_seqlens_host, sizeof(int32_t) * (num_docs + 1),
                                         cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess)
@@ -331,13 +337,81 @@ uly_status ulysses_attn_bwd(const void *q, const void *k, const void *v, const v
         return from_cuda(uly::launch_attn_bwd_f32(
             sh, static_cast<const float *>(q), static_cast<const float *>(k), static_cast<const float *>(v),
             static_cast<const float *>(o), lse, static_cast<const float *>(dout), static_cast<float *>(dq),
-            static_cast<float *>(dk), static_cast<float *>(dv), reinterpret_cast<float *>(ws + L.D_off), s));
+            static_cast<float *>(dk), static_cast<float *>(dv), reinterpret_cast<float *>(ws + W.D_off), s));
     uly::BwdScratch scr;
-    scr.lse2 = reinterpret_cast<float *>(ws + L.lse2_off);
-    scr.D = reinterpret_cast<float *>(ws + L.D_off);
-    scr.dq_acc = reinterpret_cast<float *>(ws + L.acc_off);
-    scr.Npad = L.Npad;
+    scr.lse2 = reinterpret_cast<float *>(ws + W.lse2_off);
+    scr.D = reinterpret_cast<float *>(ws + W.D_off);
+    scr.dq_acc = reinterpret_cast<float *>(ws + W.acc_off);
+    scr.Npad = W.Npad;
     return from_cuda(uly::launch_attn_bwd_bf16(sh, q, k, v, o, lse, dout, dq, dk, dv, scr, s));
+}
+
+uly::RowLayout head_rows(int64_t B, int64_t N, int32_t S) { return uly::RowLayout{0, static_cast<int>(B), N, S}; }
+
+// Arguments of the sequence-layout calls, mapped onto per-shard sizes.
+uly_status check_seq_args(int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_t d, int32_t P, uly_dtype dtype)
+{
+    if (B < 1 || N < 1 || P < 1 || Hq < 1 || Hkv < 1)
+        return ULY_ERR_INVALID_ARG;
+    if (N % P != 0 || Hq % P != 0 || Hkv % P != 0 || P > Hkv)
+        return ULY_ERR_INVALID_ARG;
+    // a 128-token tile must not straddle two sequence shards
+    if (dtype == ULY_BF16 && (N / P) % 128 != 0)
+        return ULY_ERR_UNSUPPORTED;
+    (void)d;
+    return ULY_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+uly_status ulysses_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B, int64_t N,
+                            int32_t Hq_local, int32_t Hkv_local, int32_t d, int32_t num_shards, int32_t causal,
+                            const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale, uly_dtype dtype,
+                            void *workspace, size_t workspace_bytes, void *stream)
+{
+    return attn_fwd_impl(q, k, v, o, lse, B, N, Hq_local, Hkv_local, d, num_shards, causal, cu_seqlens_host,
+                         num_docs, softmax_scale, dtype, workspace, workspace_bytes, stream,
+                         head_rows(B, N, num_shards));
+}
+
+uly_status ulysses_attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                            const void *dout, void *dq, void *dk, void *dv, int64_t B, int64_t N, int32_t Hq_local,
+                            int32_t Hkv_local, int32_t d, int32_t num_shards, int32_t causal,
+                            const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale, uly_dtype dtype,
+                            void *workspace, size_t workspace_bytes, void *stream)
+{
+    return attn_bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, N, Hq_local, Hkv_local, d, num_shards, causal,
+                         cu_seqlens_host, num_docs, softmax_scale, dtype, workspace, workspace_bytes, stream,
+                         head_rows(B, N, num_shards));
+}
+
+uly_status ulysses_attn_fwd_seq(const void *q_seq, const void *k_seq, const void *v_seq, void *o_seq, float *lse,
+                                int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int32_t causal,
+                                const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale,
+                                uly_dtype dtype, void *workspace, size_t workspace_bytes, void *stream)
+{
+    const uly_status st = check_seq_args(B, N, Hq, Hkv, d, P, dtype);
+    if (st != ULY_OK)
+        return st;
+    return attn_fwd_impl(q_seq, k_seq, v_seq, o_seq, lse, B, N, Hq / P, Hkv / P, d, P, causal, cu_seqlens_host,
+                         num_docs, softmax_scale, dtype, workspace, workspace_bytes, stream,
+                         uly::RowLayout{1, static_cast<int>(B), N / P, P});
+}
+
+uly_status ulysses_attn_bwd_seq(const void *q_seq, const void *k_seq, const void *v_seq, const void *o_seq,
+                                const float *lse, const void *dout_seq, void *dq_seq, void *dk_seq, void *dv_seq,
+                                int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int32_t causal,
+                                const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale,
+                                uly_dtype dtype, void *workspace, size_t workspace_bytes, void *stream)
+{
+    const uly_status st = check_seq_args(B, N, Hq, Hkv, d, P, dtype);
+    if (st != ULY_OK)
+        return st;
+    return attn_bwd_impl(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_seq, dv_seq, B, N, Hq / P, Hkv / P,
+                         d, P, causal, cu_seqlens_host, num_docs, softmax_scale, dtype, workspace, workspace_bytes,
+                         stream, uly::RowLayout{1, static_cast<int>(B), N / P, P});
 }
 
 uly_status ulysses_get_device_status(void *stream, uint32_t *site_out)

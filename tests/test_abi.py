@@ -107,6 +107,21 @@ def test_attn_validation(uly):
                                 1 << 30, None) == INVALID
 
 
+def test_seq_layout_validation(uly):
+    lib = uly.load()
+    p = 1 << 20
+
+    def fwd_seq(B=1, N=1024, Hq=8, Hkv=4, d=128, P=4, dt=BF16, q=p):
+        return lib.ulysses_attn_fwd_seq(q, p, p, p, p, B, N, Hq, Hkv, d, P, 1, None, 0, 0.0, dt, p, 1 << 30, None)
+
+    assert fwd_seq(N=1026) == INVALID            # N not a multiple of P
+    assert fwd_seq(Hkv=2) == INVALID             # KV heads not divisible by P
+    assert fwd_seq(Hq=6, Hkv=4, P=2) == INVALID  # local GQA group not integral
+    assert fwd_seq(N=4 * 200) == UNSUPPORTED     # bf16 tile would straddle two shards
+    assert fwd_seq(N=4 * 200, dt=FP32, d=64, q=p + 4) == MISALIGNED   # fp32 has no tile rule
+    assert fwd_seq(q=p + 4) == MISALIGNED
+
+
 def test_wait_limit_validation(uly):
     lib = uly.load()
     assert lib.ulysses_set_wait_limit_ns(10) == INVALID
