@@ -271,6 +271,44 @@ def run_ours(args, rank, world, dist):
     e2e_ms = e0.elapsed_time(e1) / e_steps
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
 
+    # ---- the sequence-parallel loss on the same tokens (Qwen3 vocabulary)
+    loss = None
+    if not args.no_loss and full:
+        V = args.vocab
+        del h_in, h_out
+        torch.cuda.empty_cache()
+        g = torch.Generator(device=dev)
+        g.manual_seed(args.seed + 7)
+        logits = torch.randn(P, B, N // P, V, device=dev, dtype=torch.bfloat16, generator=g)
+        labels = torch.randint(0, V, (P, B, N // P), device=dev, generator=g)
+        dlogits = torch.empty_like(logits)
+        ws_l = torch.empty(uly.load().ulysses_sharded_ce_workspace_size(B, N, P), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            uly.ulysses_sharded_ce_loss(logits, labels, P, dlogits=dlogits, workspace=ws_l)
+        barrier()
+        l0 = torch.cuda.Event(enable_timing=True)
+        l1 = torch.cuda.Event(enable_timing=True)
+        l0.record(stream)
+        n_rep = 3
+        for _ in range(n_rep):
+            uly.ulysses_sharded_ce_loss(logits, labels, P, dlogits=dlogits, workspace=ws_l)
+        l1.record(stream)
+        barrier()
+        loss_ms = l0.elapsed_time(l1) / n_rep
+        st, site = uly.ulysses_get_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} at site {site:#x} in the loss timing")
+        alg = 2 * logits.numel() * logits.element_size()  # read the logits once, write the gradient once
+        loss = {"what": "ulysses_sharded_ce_loss with the gradient: shifted labels, per-rank CE, "
+                        "good-token-weighted aggregation, d loss / d logits",
+                "tokens": B * N, "vocab": V, "dtype": "bf16", "ms": round(loss_ms, 3),
+                "algorithmic_bytes": alg, "gbps": round(alg / (loss_ms * 1e-3) / 1e9, 1),
+                "frac_of_hbm": round(alg / (loss_ms * 1e-3) / 1e9 / _peaks()[0], 3),
+                "note": "rows of 151936 logits do not fit on chip, so each row is read a second time "
+                        "for the gradient (3 passes of HBM traffic against 2 algorithmic)"}
+        del logits, labels, dlogits, ws_l
+        torch.cuda.empty_cache()
+
     fwd_flops, bwd_flops = _flops(w, cu)
     step_flops = fwd_flops + bwd_flops
     ms = elapsed_ms / args.steps
@@ -326,6 +364,7 @@ def run_ours(args, rank, world, dist):
             "ms_per_step": round(fused["ms_per_step"], 3),
             "value": round(whole_job_throughput(world, step_flops, fused["ms_per_step"]), 2), "unit": UNIT,
             "tokens_per_s": round(world * B * N / (fused["ms_per_step"] * 1e-3), 1)},
+        "sharded_loss": loss,
         "clocks": clk.summary(),
         "gpu_launches": args.steps * ((8 if full else 4) + 1 + 3),
     }
@@ -407,6 +446,8 @@ def main():
                     help="override the workload's N (profiling smaller cases of the same kernels)")
     ap.add_argument("--oracle-rows", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-loss", action="store_true", help="skip the sequence-parallel loss measurement")
+    ap.add_argument("--vocab", type=int, default=151936, help="vocabulary of the loss measurement (Qwen3)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

@@ -218,6 +218,41 @@ uly_status ulysses_attn_bwd_noalloc(const void *q, const void *k, const void *v,
                                     const int32_t *cu_seqlens_host, int32_t num_docs,
                                     float softmax_scale, uly_dtype dtype, void *stream);
 
+/* -------------------------------------------------------- sharded loss */
+
+/* Bytes of device workspace ulysses_sharded_ce_loss needs (0 if invalid). */
+size_t ulysses_sharded_ce_workspace_size(int64_t B, int64_t N, int32_t P);
+
+/*
+ * Next-token cross entropy of a sequence-parallel batch and its
+ * good-token-weighted aggregation across the P ranks (Accelerate PR
+ * "Deepspeed Ulysses/ALST integration", user API step 2: shift_labels, the
+ * per-rank loss, all_gather of losses and good-token counts, then
+ * sum_r loss_r * good_r / max(sum_r good_r, 1); the Transformers docs list
+ * label shifting and loss aggregation among what the Trainer does for SP).
+ *
+ * Labels are shifted over the WHOLE sequence before sharding: the target of
+ * the last token of rank r's chunk is the first label of rank r+1's chunk;
+ * the last token of each sequence gets -100 (ignored).
+ *
+ * logits     : device, [P][B][N/P][V] (each rank's LM-head output), read.
+ * labels     : device int64, [P][B][N/P], unshifted; -100 = ignored.  Values
+ *              outside [0, V) other than -100 are ignored and reported as
+ *              ULY_ERR_INVALID_ARG by ulysses_get_device_status.
+ * dlogits    : device, like logits, or NULL.  If given, receives
+ *              d total_loss / d logits = (softmax - onehot(target)) / max(T, 1)
+ *              on good rows and 0 on ignored rows (T = all good tokens).
+ * shard_loss : device fp32 [P]: rank r's mean CE over its good tokens (0 if none).
+ * shard_good : device int64 [P]: rank r's good-token count.
+ * total_loss : device fp32 [1]: the aggregated loss.
+ * workspace  : device, >= ulysses_sharded_ce_workspace_size(B, N, P).
+ * N % P == 0 (sequences padded to a multiple of the SP size).
+ */
+uly_status ulysses_sharded_ce_loss(const void *logits, const int64_t *labels, void *dlogits,
+                                   float *shard_loss, int64_t *shard_good, float *total_loss,
+                                   int64_t B, int64_t N, int32_t V, int32_t P, uly_dtype dtype,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
 /* ------------------------------------------------------------ diagnostics */
 
 /*

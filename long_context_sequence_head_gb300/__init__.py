@@ -33,7 +33,8 @@ _STATUS = {0: "ULY_OK", 1: "ULY_ERR_INVALID_ARG", 2: "ULY_ERR_UNSUPPORTED", 3: "
 # every symbol include/ulysses.h declares
 EXPORTED = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_workspace_size",
             "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_attn_fwd_seq", "ulysses_attn_bwd_seq",
-            "ulysses_attn_bwd_noalloc", "ulysses_get_device_status",
+            "ulysses_attn_bwd_noalloc", "ulysses_sharded_ce_workspace_size", "ulysses_sharded_ce_loss",
+            "ulysses_get_device_status",
             "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout",
             "ulysses_status_string", "ulysses_version")
 
@@ -74,6 +75,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.ulysses_attn_fwd_seq.argtypes = lib.ulysses_attn_fwd.argtypes
     lib.ulysses_attn_bwd_seq.argtypes = lib.ulysses_attn_bwd.argtypes
     lib.ulysses_attn_bwd_noalloc.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp]
+    lib.ulysses_sharded_ce_workspace_size.argtypes = [i64, i64, i32]
+    lib.ulysses_sharded_ce_workspace_size.restype = sz
+    lib.ulysses_sharded_ce_loss.argtypes = [vp] * 6 + [i64, i64, i32, i32, i32, vp, sz, vp]
+    lib.ulysses_sharded_ce_loss.restype = i32
     lib.ulysses_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.ulysses_set_wait_limit_ns.argtypes = [u64]
     lib.ulysses_selftest_wait_timeout.argtypes = [u64, vp]
@@ -251,6 +256,36 @@ def ulysses_attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = T
         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, N, Hq, Hkv, d, S, int(bool(causal)), cu_p, nd,
         float(softmax_scale), _dt(q), _stream(stream)))
     return dq, dk, dv
+
+
+# ---------------------------------------------------------- sharded loss
+
+def ulysses_sharded_ce_loss(logits, labels, P: int, dlogits: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None, stream=None):
+    """Shifted next-token CE per rank and its good-token-weighted aggregation.
+
+    logits [P][B][N/P][V] (bf16/fp32), labels [P][B][N/P] int64 (unshifted,
+    -100 = ignored).  Returns (shard_loss [P] fp32, shard_good [P] int64,
+    total [1] fp32) on the device; fills dlogits (like logits) if given.
+    """
+    _dev(logits, labels)
+    if dlogits is not None:
+        _dev(dlogits)
+    Ps, B, Np, V = logits.shape
+    N = Np * P
+    if labels.dtype != torch.int64 or tuple(labels.shape) != (P, B, Np):
+        raise ValueError("labels must be int64 [P][B][N/P]")
+    dev = logits.device
+    shard_loss = torch.empty(P, dtype=torch.float32, device=dev)
+    shard_good = torch.empty(P, dtype=torch.int64, device=dev)
+    total = torch.empty(4, dtype=torch.float32, device=dev)
+    need = int(load().ulysses_sharded_ce_workspace_size(B, N, P))
+    ws = _workspace(workspace, need, dev)
+    _check("ulysses_sharded_ce_loss", load().ulysses_sharded_ce_loss(
+        logits.data_ptr(), labels.data_ptr(), dlogits.data_ptr() if dlogits is not None else None,
+        shard_loss.data_ptr(), shard_good.data_ptr(), total.data_ptr(), B, N, V, P, _dt(logits),
+        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
+    return shard_loss, shard_good, total[:1]
 
 
 # ------------------------------------------------------------ diagnostics

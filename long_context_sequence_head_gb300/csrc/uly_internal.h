@@ -101,4 +101,10 @@ cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *
 
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, cudaStream_t stream);
 
+// ------------------------------------------------------- sharded loss
+cudaError_t launch_sharded_ce(const void *logits, const int64_t *labels, void *dlogits, float *shard_loss,
+                              int64_t *shard_good, float *total, int64_t B, int64_t N, int64_t V, int P, int esize,
+                              void *workspace, cudaStream_t stream);
+size_t sharded_ce_workspace(int64_t B, int64_t N, int P);
+
 }  // namespace uly

@@ -414,6 +414,38 @@ uly_status ulysses_attn_bwd_seq(const void *q_seq, const void *k_seq, const void
                          stream, uly::RowLayout{1, static_cast<int>(B), N / P, P});
 }
 
+size_t ulysses_sharded_ce_workspace_size(int64_t B, int64_t N, int32_t P)
+{
+    if (B < 1 || N < 1 || P < 1 || N % P != 0)
+        return 0;
+    return uly::sharded_ce_workspace(B, N, P);
+}
+
+uly_status ulysses_sharded_ce_loss(const void *logits, const int64_t *labels, void *dlogits, float *shard_loss,
+                                   int64_t *shard_good, float *total_loss, int64_t B, int64_t N, int32_t V,
+                                   int32_t P, uly_dtype dtype, void *workspace, size_t workspace_bytes,
+                                   void *stream)
+{
+    if (!logits || !labels || !shard_loss || !shard_good || !total_loss || !workspace)
+        return ULY_ERR_INVALID_ARG;
+    if (B < 1 || N < 1 || P < 1 || V < 1 || N % P != 0 || esize_of(dtype) == 0)
+        return ULY_ERR_INVALID_ARG;
+    if (B * N > (int64_t(1) << 31) - 1)
+        return ULY_ERR_UNSUPPORTED;
+    if (!aligned16(logits) || !aligned16(labels) || !aligned16(shard_loss) || !aligned16(shard_good) ||
+        !aligned16(total_loss) || !aligned16(workspace) || (dlogits != nullptr && !aligned16(dlogits)))
+        return ULY_ERR_MISALIGNED;
+    const size_t bytes = static_cast<size_t>(B) * N * V * esize_of(dtype);
+    if (dlogits != nullptr && overlap(logits, bytes, dlogits, bytes))
+        return ULY_ERR_OVERLAP;
+    if (workspace_bytes < uly::sharded_ce_workspace(B, N, P))
+        return ULY_ERR_WORKSPACE;
+    if (uly::device_status_ptr() == nullptr)
+        return ULY_ERR_CUDA;
+    return from_cuda(uly::launch_sharded_ce(logits, labels, dlogits, shard_loss, shard_good, total_loss, B, N, V, P,
+                                            esize_of(dtype), workspace, static_cast<cudaStream_t>(stream)));
+}
+
 uly_status ulysses_get_device_status(void *stream, uint32_t *site_out)
 {
     unsigned *p = uly::device_status_ptr();

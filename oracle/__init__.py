@@ -23,8 +23,9 @@ from typing import Optional, Sequence
 import numpy as np
 import torch
 
-from .loss import (aggregate_sharded_loss, full_sequence_loss,  # noqa: F401
-                   per_rank_losses, shift_labels)
+from .loss import (aggregate_sharded_loss, aggregated_loss_grad,  # noqa: F401
+                   full_sequence_loss, per_rank_losses, per_rank_losses_batched, shift_labels,
+                   shift_labels_batched)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")

@@ -67,3 +67,57 @@ def full_sequence_loss(logits: np.ndarray, shifted: np.ndarray) -> float:
             total += _token_ce(logits[i], int(shifted[i]))
             good += 1
     return total / max(good, 1)
+
+
+# ------------------------------------------------------------------ batched
+# The Trainer shards every row of the local batch the same way: rank r holds
+# tokens [r*N/P, (r+1)*N/P) of each of the B rows, and its loss is the mean
+# over all of its good tokens (all rows).
+
+def shift_labels_batched(labels: np.ndarray) -> np.ndarray:
+    """labels [B][N] -> next-token labels per row, last of each row -100."""
+    labels = np.asarray(labels, dtype=np.int64)
+    return np.stack([shift_labels(row) for row in labels])
+
+
+def per_rank_losses_batched(logits: np.ndarray, shifted: np.ndarray, P: int):
+    """logits [B][N][V], shifted [B][N] -> per-rank mean CE and good counts."""
+    B, N = shifted.shape
+    assert N % P == 0
+    Np = N // P
+    losses, goods = [], []
+    for r in range(P):
+        total, good = 0.0, 0
+        for b in range(B):
+            for i in range(r * Np, (r + 1) * Np):
+                if shifted[b, i] != IGNORE:
+                    total += _token_ce(logits[b, i], int(shifted[b, i]))
+                    good += 1
+        losses.append(total / good if good > 0 else 0.0)
+        goods.append(good)
+    return losses, goods
+
+
+def aggregated_loss_grad(logits: np.ndarray, shifted: np.ndarray, P: int) -> np.ndarray:
+    """Gradient of the aggregated loss with respect to logits [B][N][V].
+
+    total = sum_r loss_r * good_r / max(T, 1) with loss_r = (sum of CE over
+    rank r's good tokens) / good_r, so total = (sum of CE over all good
+    tokens) / max(T, 1) and d total / d logit[b, i, :] = (softmax(logit[b,i]) -
+    onehot(label)) / max(T, 1) for good tokens, 0 for ignored ones.
+    """
+    logits = np.asarray(logits, dtype=np.float64)
+    B, N, V = logits.shape
+    T = int((shifted != IGNORE).sum())
+    g = np.zeros_like(logits)
+    for b in range(B):
+        for i in range(N):
+            y = int(shifted[b, i])
+            if y == IGNORE:
+                continue
+            row = logits[b, i]
+            e = np.exp(row - row.max())
+            g[b, i] = e / e.sum()
+            g[b, i, y] -= 1.0
+            g[b, i] /= max(T, 1)
+    return g

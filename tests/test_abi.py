@@ -122,6 +122,20 @@ def test_seq_layout_validation(uly):
     assert fwd_seq(q=p + 4) == MISALIGNED
 
 
+def test_sharded_ce_validation(uly):
+    lib = uly.load()
+    p = 1 << 20
+    ws = lib.ulysses_sharded_ce_workspace_size
+    assert ws(1, 64, 4) > 0 and ws(1, 65, 4) == 0
+    call = lambda N=64, P=4, V=100, dt=BF16, lg=p, dl=None, wsb=1 << 30: lib.ulysses_sharded_ce_loss(
+        lg, p, dl, p, p, p, 1, N, V, P, dt, p, wsb, None)
+    assert call(N=65) == INVALID          # not padded to a multiple of P
+    assert call(V=0) == INVALID
+    assert call(lg=p + 2) == MISALIGNED
+    assert call(dl=p) == OVERLAP           # gradient would overwrite the logits
+    assert call(wsb=8) == WORKSPACE
+
+
 def test_wait_limit_validation(uly):
     lib = uly.load()
     assert lib.ulysses_set_wait_limit_ns(10) == INVALID

@@ -60,3 +60,48 @@ def test_shift_before_sharding_crosses_boundaries(oracle_mod):
     # sharding first and shifting inside each shard would lose that target
     losses, goods = oracle_mod.per_rank_losses(logits, shifted, P)
     assert sum(goods) == N - 1
+
+
+def test_batched_reduces_to_single_row(oracle_mod):
+    N, V, P = 16, 5, 4
+    logits, labels = draw_labels_logits(N, V, 21, ignore_frac=0.2)
+    sh = oracle_mod.shift_labels(labels)
+    l1, g1 = oracle_mod.per_rank_losses(logits, sh, P)
+    l2, g2 = oracle_mod.per_rank_losses_batched(logits[None], oracle_mod.shift_labels_batched(labels[None]), P)
+    assert g1 == g2 and np.allclose(l1, l2, rtol=0, atol=0)
+
+
+def test_batched_aggregate_equals_torch_mean(oracle_mod):
+    B, N, V, P = 3, 12, 7, 4
+    rng = np.random.default_rng(5)
+    logits = rng.standard_normal((B, N, V))
+    labels = rng.integers(0, V, size=(B, N))
+    labels[rng.random((B, N)) < 0.3] = -100
+    sh = oracle_mod.shift_labels_batched(labels)
+    losses, goods = oracle_mod.per_rank_losses_batched(logits, sh, P)
+    agg = oracle_mod.aggregate_sharded_loss(losses, goods)
+    ref = F.cross_entropy(torch.from_numpy(logits).reshape(-1, V), torch.from_numpy(sh).reshape(-1),
+                          ignore_index=-100, reduction="mean")
+    assert agg == pytest.approx(float(ref), rel=1e-12)
+
+
+def test_aggregated_grad_matches_autograd_and_finite_differences(oracle_mod):
+    B, N, V, P = 2, 8, 5, 2
+    rng = np.random.default_rng(9)
+    logits = rng.standard_normal((B, N, V))
+    labels = rng.integers(0, V, size=(B, N))
+    labels[0, 2] = -100
+    sh = oracle_mod.shift_labels_batched(labels)
+    g = oracle_mod.aggregated_loss_grad(logits, sh, P)
+    lt = torch.from_numpy(logits.copy()).requires_grad_()
+    F.cross_entropy(lt.reshape(-1, V), torch.from_numpy(sh).reshape(-1), ignore_index=-100).backward()
+    np.testing.assert_allclose(g, lt.grad.numpy(), rtol=1e-12, atol=1e-14)
+
+    def total(x):
+        l, c = oracle_mod.per_rank_losses_batched(x, sh, P)
+        return oracle_mod.aggregate_sharded_loss(l, c)
+    h = 1e-6
+    for idx in [(0, 0, 1), (1, 5, 4), (0, 7, 0), (0, 2, 3)]:
+        x = logits.copy(); x[idx] += h
+        y = logits.copy(); y[idx] -= h
+        assert (total(x) - total(y)) / (2 * h) == pytest.approx(g[idx], abs=1e-8)
