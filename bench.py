@@ -246,6 +246,46 @@ def run_ours(args, rank, world, dist):
         if st != 0:
             raise RuntimeError(f"device status {st} at site {site:#x} in the fused timing")
 
+    # ---- ring attention on the same inputs (chunks of the seq layout, all heads)
+    ring = None
+    if full and not args.no_ring:
+        Np = N // P
+        lse_r = torch.empty(P, B, w.Hq, Np, dtype=torch.float32, device=dev)
+        ws_rf = torch.empty(uly.load().ulysses_ring_attn_workspace_size(B, N, w.Hq, w.Hkv, d, P, 0,
+                                                                       0 if bt == torch.bfloat16 else 1),
+                            dtype=torch.uint8, device=dev)
+        ws_rb = torch.empty(uly.load().ulysses_ring_attn_workspace_size(B, N, w.Hq, w.Hkv, d, P, 1,
+                                                                       0 if bt == torch.bfloat16 else 1),
+                            dtype=torch.uint8, device=dev)
+
+        def ring_step():
+            uly.ulysses_ring_attn_fwd(q, k, v, o_seq, lse_r, P, causal=w.causal, workspace=ws_rf)
+            uly.ulysses_ring_attn_bwd(q, k, v, o_seq, lse_r, do, dq_seq, dk_seq, dv_seq, P, causal=w.causal,
+                                      workspace=ws_rb)
+        for _ in range(2):
+            ring_step()
+        barrier()
+        r0 = torch.cuda.Event(enable_timing=True)
+        r1 = torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for _ in range(args.steps):
+            ring_step()
+        r1.record(stream)
+        barrier()
+        ring_ms = max_over_ranks(r0.elapsed_time(r1) / args.steps, dist, dev)
+        st, site = uly.ulysses_get_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} at site {site:#x} in the ring timing")
+        es = 2 if bt == torch.bfloat16 else 4
+        ring = {"ms_per_step": ring_ms}
+        # per GPU and layer, forward + backward, if the P ranks were P GPUs:
+        #   Ulysses: the four all-to-alls move (P-1)/P of the local Q,K,V,O and dO,dQ,dK,dV
+        #   ring:    P-1 hops of the K,V chunk forward; K,V and the fp32 dK,dV accumulators backward
+        ring["comm_model_bytes_per_gpu"] = {
+            "ulysses": int((P - 1) / P * Np * B * 4 * (w.Hq + w.Hkv) * d * es),
+            "ring": int((P - 1) * Np * B * 2 * w.Hkv * d * (es + es + 4))}
+        del ws_rf, ws_rb, lse_r
+
     # ---- end to end: host buffers in pinned memory, copies inside the timed region
     pin = lambda x: torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     h_in = {n: pin(x).copy_(x) for n, x in (("q", q), ("k", k), ("v", v), ("dout", do))}
@@ -364,6 +404,12 @@ def run_ours(args, rank, world, dist):
             "ms_per_step": round(fused["ms_per_step"], 3),
             "value": round(whole_job_throughput(world, step_flops, fused["ms_per_step"]), 2), "unit": UNIT,
             "tokens_per_s": round(world * B * N / (fused["ms_per_step"] * 1e-3), 1)},
+        "ring_attention": None if ring is None else {
+            "what": "ulysses_ring_attn_fwd + ulysses_ring_attn_bwd on the same inputs: P chunks of all heads, "
+                    "P ring steps merged through the log-sum-exp (one GPU: the hops are pointer offsets)",
+            "ms_per_step": round(ring["ms_per_step"], 3),
+            "value": round(whole_job_throughput(world, step_flops, ring["ms_per_step"]), 2), "unit": UNIT,
+            "comm_model_bytes_per_gpu_per_layer": ring["comm_model_bytes_per_gpu"]},
         "sharded_loss": loss,
         "clocks": clk.summary(),
         "gpu_launches": args.steps * ((8 if full else 4) + 1 + 3),
@@ -447,6 +493,7 @@ def main():
     ap.add_argument("--oracle-rows", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-loss", action="store_true", help="skip the sequence-parallel loss measurement")
+    ap.add_argument("--no-ring", action="store_true", help="skip the ring-attention measurement")
     ap.add_argument("--vocab", type=int, default=151936, help="vocabulary of the loss measurement (Qwen3)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))

@@ -218,6 +218,41 @@ uly_status ulysses_attn_bwd_noalloc(const void *q, const void *k, const void *v,
                                     const int32_t *cu_seqlens_host, int32_t num_docs,
                                     float softmax_scale, uly_dtype dtype, void *stream);
 
+/* --------------------------------------------------------- ring attention */
+
+/*
+ * Ring attention over P virtual ranks, the pages' alternative to Ulysses
+ * ("Sequence Parallelism for Long-Context AI Training", "Advanced Scaling:
+ * Ring Attention and Ulysses"; blog summary, "Comparing Ulysses and Ring
+ * Attention"): rank r keeps its chunk of Q for ALL heads and the K/V chunks
+ * travel round the ring; in P steps every query chunk meets every key chunk
+ * (step k: query chunk r with key chunk (r - k) mod P; causal keeps only
+ * r >= k after step 0), and the partial results are merged through their
+ * log-sum-exp.  The result equals causal attention over all N tokens, i.e.
+ * the same as the Ulysses path, without any head sharding.
+ *
+ * q_seq, o_seq, dout_seq, dq_seq : device, [P][B][N/P][Hq][d]
+ * k_seq, v_seq, dk_seq, dv_seq   : device, [P][B][N/P][Hkv][d]
+ * lse : device fp32, [P][B][Hq][N/P] (chunk, batch, head, position in chunk)
+ * Hq, Hkv are the total head counts (ring attention does not shard heads).
+ * N % P == 0; otherwise the rules of ulysses_attn_fwd on each chunk
+ * (N/P tokens), without packed documents.
+ * workspace : device, >= ulysses_ring_attn_workspace_size(..., for_bwd).
+ * The backward uses the final o and lse of the forward.
+ */
+size_t ulysses_ring_attn_workspace_size(int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_t d,
+                                        int32_t P, int32_t for_bwd, uly_dtype dtype);
+uly_status ulysses_ring_attn_fwd(const void *q_seq, const void *k_seq, const void *v_seq, void *o_seq,
+                                 float *lse, int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_t d,
+                                 int32_t P, int32_t causal, float softmax_scale, uly_dtype dtype,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+uly_status ulysses_ring_attn_bwd(const void *q_seq, const void *k_seq, const void *v_seq,
+                                 const void *o_seq, const float *lse, const void *dout_seq,
+                                 void *dq_seq, void *dk_seq, void *dv_seq, int64_t B, int64_t N,
+                                 int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int32_t causal,
+                                 float softmax_scale, uly_dtype dtype, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
 /* -------------------------------------------------------- sharded loss */
 
 /* Bytes of device workspace ulysses_sharded_ce_loss needs (0 if invalid). */

@@ -34,6 +34,7 @@ _STATUS = {0: "ULY_OK", 1: "ULY_ERR_INVALID_ARG", 2: "ULY_ERR_UNSUPPORTED", 3: "
 EXPORTED = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_workspace_size",
             "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_attn_fwd_seq", "ulysses_attn_bwd_seq",
             "ulysses_attn_bwd_noalloc", "ulysses_sharded_ce_workspace_size", "ulysses_sharded_ce_loss",
+            "ulysses_ring_attn_workspace_size", "ulysses_ring_attn_fwd", "ulysses_ring_attn_bwd",
             "ulysses_get_device_status",
             "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout",
             "ulysses_status_string", "ulysses_version")
@@ -75,6 +76,12 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.ulysses_attn_fwd_seq.argtypes = lib.ulysses_attn_fwd.argtypes
     lib.ulysses_attn_bwd_seq.argtypes = lib.ulysses_attn_bwd.argtypes
     lib.ulysses_attn_bwd_noalloc.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp]
+    lib.ulysses_ring_attn_workspace_size.argtypes = [i64, i64, i32, i32, i32, i32, i32, i32]
+    lib.ulysses_ring_attn_workspace_size.restype = sz
+    lib.ulysses_ring_attn_fwd.argtypes = [vp] * 5 + [i64, i64, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
+    lib.ulysses_ring_attn_fwd.restype = i32
+    lib.ulysses_ring_attn_bwd.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
+    lib.ulysses_ring_attn_bwd.restype = i32
     lib.ulysses_sharded_ce_workspace_size.argtypes = [i64, i64, i32]
     lib.ulysses_sharded_ce_workspace_size.restype = sz
     lib.ulysses_sharded_ce_loss.argtypes = [vp] * 6 + [i64, i64, i32, i32, i32, vp, sz, vp]
@@ -256,6 +263,42 @@ def ulysses_attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = T
         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, N, Hq, Hkv, d, S, int(bool(causal)), cu_p, nd,
         float(softmax_scale), _dt(q), _stream(stream)))
     return dq, dk, dv
+
+
+# -------------------------------------------------------- ring attention
+
+def ulysses_ring_attn_fwd(q_seq, k_seq, v_seq, o_seq, lse, P: int, causal: bool = True,
+                          softmax_scale: float = 0.0, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Ring attention over P chunks of the sequence-sharded layout; lse [P][B][Hq][N/P]."""
+    _dev(q_seq, k_seq, v_seq, o_seq, lse)
+    Ps, B, Np, Hq, d = q_seq.shape
+    Hkv = k_seq.shape[3]
+    N = Np * P
+    need = int(load().ulysses_ring_attn_workspace_size(B, N, Hq, Hkv, d, P, 0, _dt(q_seq)))
+    ws = _workspace(workspace, need, q_seq.device)
+    _check("ulysses_ring_attn_fwd", load().ulysses_ring_attn_fwd(
+        q_seq.data_ptr(), k_seq.data_ptr(), v_seq.data_ptr(), o_seq.data_ptr(), lse.data_ptr(), B, N, Hq, Hkv,
+        d, P, int(bool(causal)), float(softmax_scale), _dt(q_seq), ws.data_ptr(),
+        ws.numel() * ws.element_size(), _stream(stream)))
+    return o_seq, lse
+
+
+def ulysses_ring_attn_bwd(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_seq, dv_seq, P: int,
+                          causal: bool = True, softmax_scale: float = 0.0,
+                          workspace: Optional[torch.Tensor] = None, stream=None):
+    """Backward of ulysses_ring_attn_fwd (final o and lse)."""
+    _dev(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_seq, dv_seq)
+    Ps, B, Np, Hq, d = q_seq.shape
+    Hkv = k_seq.shape[3]
+    N = Np * P
+    need = int(load().ulysses_ring_attn_workspace_size(B, N, Hq, Hkv, d, P, 1, _dt(q_seq)))
+    ws = _workspace(workspace, need, q_seq.device)
+    _check("ulysses_ring_attn_bwd", load().ulysses_ring_attn_bwd(
+        q_seq.data_ptr(), k_seq.data_ptr(), v_seq.data_ptr(), o_seq.data_ptr(), lse.data_ptr(),
+        dout_seq.data_ptr(), dq_seq.data_ptr(), dk_seq.data_ptr(), dv_seq.data_ptr(), B, N, Hq, Hkv, d, P,
+        int(bool(causal)), float(softmax_scale), _dt(q_seq), ws.data_ptr(), ws.numel() * ws.element_size(),
+        _stream(stream)))
+    return dq_seq, dk_seq, dv_seq
 
 
 # ---------------------------------------------------------- sharded loss

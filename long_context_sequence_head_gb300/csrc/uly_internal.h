@@ -108,3 +108,31 @@ cudaError_t launch_sharded_ce(const void *logits, const int64_t *labels, void *d
 size_t sharded_ce_workspace(int64_t B, int64_t N, int P);
 
 }  // namespace uly
+
+#include <ulysses.h>
+
+namespace uly {
+
+// Validated attention calls (ulysses_api.cu), shared by the C entry points
+// and the ring-attention orchestration.
+uly_status attn_fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B, int64_t N,
+                         int32_t Hq_local, int32_t Hkv_local, int32_t d, int32_t num_shards, int32_t causal,
+                         const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale, uly_dtype dtype,
+                         void *workspace, size_t workspace_bytes, void *stream, RowLayout L);
+uly_status attn_bwd_impl(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                         const void *dout, void *dq, void *dk, void *dv, int64_t B, int64_t N, int32_t Hq_local,
+                         int32_t Hkv_local, int32_t d, int32_t num_shards, int32_t causal,
+                         const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale, uly_dtype dtype,
+                         void *workspace, size_t workspace_bytes, void *stream, RowLayout L);
+RowLayout head_rows(int64_t B, int64_t N, int32_t S);
+
+// ring attention (ring.cu)
+size_t ring_workspace_size(int64_t B, int64_t N, int Hq, int Hkv, int d, int P, bool bwd, uly_dtype dt);
+uly_status ring_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B, int64_t N, int Hq,
+                    int Hkv, int d, int P, int causal, float scale, uly_dtype dt, void *workspace, size_t ws_bytes,
+                    cudaStream_t s);
+uly_status ring_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
+                    void *dq, void *dk, void *dv, int64_t B, int64_t N, int Hq, int Hkv, int d, int P, int causal,
+                    float scale, uly_dtype dt, void *workspace, size_t ws_bytes, cudaStream_t s);
+
+}  // namespace uly

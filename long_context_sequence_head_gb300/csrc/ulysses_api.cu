@@ -244,7 +244,7 @@ size_t ulysses_attn_workspace_size(int64_t B, int64_t N, int32_t Hq_local, int32
 
 }  // extern "C"
 
-namespace {
+namespace uly {
 
 uly_status attn_fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B, int64_t N,
                          int32_t Hq_local, int32_t Hkv_local, int32_t d, int32_t num_shards, int32_t causal,
@@ -348,6 +348,10 @@ uly_status attn_bwd_impl(const void *q, const void *k, const void *v, const void
 
 uly::RowLayout head_rows(int64_t B, int64_t N, int32_t S) { return uly::RowLayout{0, static_cast<int>(B), N, S}; }
 
+}  // namespace uly
+
+namespace {
+
 // Arguments of the sequence-layout calls, mapped onto per-shard sizes.
 uly_status check_seq_args(int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_t d, int32_t P, uly_dtype dtype)
 {
@@ -371,9 +375,9 @@ uly_status ulysses_attn_fwd(const void *q, const void *k, const void *v, void *o
                             const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale, uly_dtype dtype,
                             void *workspace, size_t workspace_bytes, void *stream)
 {
-    return attn_fwd_impl(q, k, v, o, lse, B, N, Hq_local, Hkv_local, d, num_shards, causal, cu_seqlens_host,
+    return uly::attn_fwd_impl(q, k, v, o, lse, B, N, Hq_local, Hkv_local, d, num_shards, causal, cu_seqlens_host,
                          num_docs, softmax_scale, dtype, workspace, workspace_bytes, stream,
-                         head_rows(B, N, num_shards));
+                         uly::head_rows(B, N, num_shards));
 }
 
 uly_status ulysses_attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
@@ -382,9 +386,9 @@ uly_status ulysses_attn_bwd(const void *q, const void *k, const void *v, const v
                             const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale, uly_dtype dtype,
                             void *workspace, size_t workspace_bytes, void *stream)
 {
-    return attn_bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, N, Hq_local, Hkv_local, d, num_shards, causal,
+    return uly::attn_bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, N, Hq_local, Hkv_local, d, num_shards, causal,
                          cu_seqlens_host, num_docs, softmax_scale, dtype, workspace, workspace_bytes, stream,
-                         head_rows(B, N, num_shards));
+                         uly::head_rows(B, N, num_shards));
 }
 
 uly_status ulysses_attn_fwd_seq(const void *q_seq, const void *k_seq, const void *v_seq, void *o_seq, float *lse,
@@ -395,7 +399,7 @@ uly_status ulysses_attn_fwd_seq(const void *q_seq, const void *k_seq, const void
     const uly_status st = check_seq_args(B, N, Hq, Hkv, d, P, dtype);
     if (st != ULY_OK)
         return st;
-    return attn_fwd_impl(q_seq, k_seq, v_seq, o_seq, lse, B, N, Hq / P, Hkv / P, d, P, causal, cu_seqlens_host,
+    return uly::attn_fwd_impl(q_seq, k_seq, v_seq, o_seq, lse, B, N, Hq / P, Hkv / P, d, P, causal, cu_seqlens_host,
                          num_docs, softmax_scale, dtype, workspace, workspace_bytes, stream,
                          uly::RowLayout{1, static_cast<int>(B), N / P, P});
 }
@@ -409,9 +413,69 @@ uly_status ulysses_attn_bwd_seq(const void *q_seq, const void *k_seq, const void
     const uly_status st = check_seq_args(B, N, Hq, Hkv, d, P, dtype);
     if (st != ULY_OK)
         return st;
-    return attn_bwd_impl(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_seq, dv_seq, B, N, Hq / P, Hkv / P,
+    return uly::attn_bwd_impl(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_seq, dv_seq, B, N, Hq / P, Hkv / P,
                          d, P, causal, cu_seqlens_host, num_docs, softmax_scale, dtype, workspace, workspace_bytes,
                          stream, uly::RowLayout{1, static_cast<int>(B), N / P, P});
+}
+
+size_t ulysses_ring_attn_workspace_size(int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_t d, int32_t P,
+                                        int32_t for_bwd, uly_dtype dtype)
+{
+    if (B < 1 || N < 1 || P < 1 || N % P != 0)
+        return 0;
+    return uly::ring_workspace_size(B, N, Hq, Hkv, d, P, for_bwd != 0, dtype);
+}
+
+namespace {
+uly_status check_ring(const void *const *ptrs, int nptr, int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_t d,
+                      int32_t P, int32_t causal, uly_dtype dtype, void *workspace, size_t ws_bytes, bool bwd)
+{
+    for (int i = 0; i < nptr; ++i)
+        if (ptrs[i] == nullptr)
+            return ULY_ERR_INVALID_ARG;
+    if (P < 1 || N < 1 || N % P != 0)
+        return ULY_ERR_INVALID_ARG;
+    const uly_status st = check_attn_args(B, N / P, Hq, Hkv, d, P, causal, nullptr, 0, dtype);
+    if (st != ULY_OK)
+        return st;
+    for (int i = 0; i < nptr; ++i)
+        if (!aligned16(ptrs[i]))
+            return ULY_ERR_MISALIGNED;
+    if (workspace == nullptr || !aligned16(workspace))
+        return workspace == nullptr ? ULY_ERR_INVALID_ARG : ULY_ERR_MISALIGNED;
+    if (ws_bytes < uly::ring_workspace_size(B, N, Hq, Hkv, d, P, bwd, dtype))
+        return ULY_ERR_WORKSPACE;
+    if (uly::tensor_map_encoder() == nullptr || uly::device_status_ptr() == nullptr)
+        return ULY_ERR_CUDA;
+    return ULY_OK;
+}
+}  // namespace
+
+uly_status ulysses_ring_attn_fwd(const void *q_seq, const void *k_seq, const void *v_seq, void *o_seq, float *lse,
+                                 int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int32_t causal,
+                                 float softmax_scale, uly_dtype dtype, void *workspace, size_t workspace_bytes,
+                                 void *stream)
+{
+    const void *ptrs[5] = {q_seq, k_seq, v_seq, o_seq, lse};
+    const uly_status st = check_ring(ptrs, 5, B, N, Hq, Hkv, d, P, causal, dtype, workspace, workspace_bytes, false);
+    if (st != ULY_OK)
+        return st;
+    return uly::ring_fwd(q_seq, k_seq, v_seq, o_seq, lse, B, N, Hq, Hkv, d, P, causal, softmax_scale, dtype,
+                         workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+uly_status ulysses_ring_attn_bwd(const void *q_seq, const void *k_seq, const void *v_seq, const void *o_seq,
+                                 const float *lse, const void *dout_seq, void *dq_seq, void *dk_seq, void *dv_seq,
+                                 int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_t d, int32_t P, int32_t causal,
+                                 float softmax_scale, uly_dtype dtype, void *workspace, size_t workspace_bytes,
+                                 void *stream)
+{
+    const void *ptrs[9] = {q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_seq, dv_seq};
+    const uly_status st = check_ring(ptrs, 9, B, N, Hq, Hkv, d, P, causal, dtype, workspace, workspace_bytes, true);
+    if (st != ULY_OK)
+        return st;
+    return uly::ring_bwd(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_seq, dv_seq, B, N, Hq, Hkv, d, P,
+                         causal, softmax_scale, dtype, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 size_t ulysses_sharded_ce_workspace_size(int64_t B, int64_t N, int32_t P)

@@ -122,6 +122,20 @@ def test_seq_layout_validation(uly):
     assert fwd_seq(q=p + 4) == MISALIGNED
 
 
+def test_ring_validation(uly):
+    lib = uly.load()
+    p = 1 << 20
+    assert lib.ulysses_ring_attn_workspace_size(1, 1024, 8, 2, 128, 4, 1, BF16) > 0
+    assert lib.ulysses_ring_attn_workspace_size(1, 1026, 8, 2, 128, 4, 1, BF16) == 0
+    call = lambda N=1024, Hq=8, Hkv=2, d=128, P=4, dt=BF16, q=p, wsb=1 << 34: lib.ulysses_ring_attn_fwd(
+        q, p, p, p, p, 1, N, Hq, Hkv, d, P, 1, 0.0, dt, p, wsb, None)
+    assert call(N=1026) == INVALID
+    assert call(Hkv=3) == INVALID
+    assert call(d=64) == UNSUPPORTED
+    assert call(q=p + 8) == MISALIGNED
+    assert call(wsb=64) == WORKSPACE
+
+
 def test_sharded_ce_validation(uly):
     lib = uly.load()
     p = 1 << 20
