@@ -390,7 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *ds_row = smem + BwdSmem::kdS + (cq >> 1) * kChunk + j * 128;
         bool ok = true;
         // dQ partial: read out of TMEM (frees the dP/dQ columns), then its 8
-        // vector reductions go out in two groups between later work
+        // vector reductions (one per group of 4 columns) are spread over the
+        // following work: groups 0-3 while the dP product runs, 4-5 after the
+        // dS^T hand-off, 6 at the top of the next iteration and 7 in the middle
+        // of its P^T computation.  Pushing 64 KB per iteration through the SM's
+        // global-reduction path in bursts stalls the warps that are due on the
+        // S -> P -> dV and dP -> dS^T chains; this spacing measured fastest.
         uint32_t xq[32];
         float *dq_base = nullptr;
         auto read_dq = [&](int it) {
@@ -410,10 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 j * 4
                           : nullptr;
         };
-        auto reduce_dq_part = [&](int part) {  // groups 4*part .. 4*part+3 of 8
+        auto reduce_groups = [&](int g0, int g1) {  // groups g0 .. g1-1 of 8
             if (dq_base != nullptr) {
 #pragma unroll
-                for (int g = 4 * part; g < 4 * part + 4; ++g)
+                for (int g = g0; g < g1; ++g)
                     red_add_v4(dq_base + g * (kBM * 4), __uint_as_float(xq[4 * g]), __uint_as_float(xq[4 * g + 1]),
                                __uint_as_float(xq[4 * g + 2]), __uint_as_float(xq[4 * g + 3]));
             }
@@ -423,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t q0 = static_cast<int64_t>(m_lo + it % n_m) * kBM;
             const float *lse_s = reinterpret_cast<const float *>(smem + BwdSmem::kLse + slot * 512) + c0;
             const float *D_s = reinterpret_cast<const float *>(smem + BwdSmem::kDv + slot * 512) + c0;
+            reduce_groups(6, 7);  // of the partial read in the previous iteration
             if (!mbar_wait_warp(s_full, it & 1, p.w, 0x71) ||
                 !mbar_wait_warp(&q_full[slot], (it >> 1) & 1, p.w, 0x72)) {
                 ok = false;
@@ -444,6 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          make_float2(-l4.z, -l4.w));
                 pk[c / 2] = pack_bf16x2(ex2_approx(x01.x), ex2_approx(x01.y));
                 pk[c / 2 + 1] = pack_bf16x2(ex2_approx(x23.x), ex2_approx(x23.y));
+                if (c == 12)
+                    reduce_groups(7, 8);
             }
             if (!((q0 + c0 >= lo) && (q0 + c0 + 32 <= hi))) {
                 // boundary tile for this key: zero the probabilities of rows
@@ -472,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 read_dq(it - 1);
-                reduce_dq_part(0);
+                reduce_groups(0, 4);
             } else {
                 dq_base = nullptr;
             }
@@ -509,14 +517,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(ds_full);
-            reduce_dq_part(1);
+            reduce_groups(4, 6);
         }
         if (ok && n_it > 0) {
             if (mbar_wait_warp(dq_full, (n_it - 1) & 1, p.w, 0x76)) {
                 tc_fence_after();
+                reduce_groups(6, 8);  // the rest of the partial before the last
                 read_dq(n_it - 1);
-                reduce_dq_part(0);
-                reduce_dq_part(1);
+                reduce_groups(0, 8);
             } else {
                 ok = false;
             }
