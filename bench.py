@@ -167,8 +167,15 @@ def run_ours(args, rank, world, dist):
                        dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     full = S == P  # the 1M workload times one head shard; swaps back then need all shards
+    q_in, k_in, v_in, do_in = q, k, v, do
+    outs_main = (o_seq, dq_seq, dk_seq, dv_seq)
 
-    def step(ev=None):
+    def step(ev=None, ins=None, outs_seq=None):
+        """One layer step on the inputs `ins` = (q, k, v, dO) in the seq layout,
+        writing (O, dQ, dK, dV) in the seq layout to `outs_seq`."""
+        q, k, v, do = ins if ins is not None else (q_in, k_in, v_in, do_in)
+        o_seq, dq_seq, dk_seq, dv_seq = outs_seq if outs_seq is not None else outs_main
+
         def mark(i):
             if ev is not None:
                 ev[i].record(stream)
@@ -286,30 +293,86 @@ def run_ours(args, rank, world, dist):
             "ring": int((P - 1) * Np * B * 2 * w.Hkv * d * (es + es + 4))}
         del ws_rf, ws_rb, lse_r
 
-    # ---- end to end: host buffers in pinned memory, copies inside the timed region
+    # ---- end to end: host buffers in pinned memory, copies inside the timed region.
+    # Every step uploads its own Q, K, V, dO from pinned host memory and reads
+    # its O, dQ, dK, dV back.  Served as a stream of batches: two sets of device
+    # buffers, the upload of step i+1 (one copy stream) and the read-back of
+    # step i-1 (another) run while step i computes; the timed region opens
+    # before the first upload and closes after the last read-back.  The same
+    # loop on one stream (no overlap) is reported beside it.
     pin = lambda x: torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-    h_in = {n: pin(x).copy_(x) for n, x in (("q", q), ("k", k), ("v", v), ("dout", do))}
-    outs = (o_seq, dq_seq, dk_seq, dv_seq) if full else (oh, dqh, dkh, dvh)
-    h_out = [pin(x) for x in outs]
-    h2d = sum(x.numel() * x.element_size() for x in h_in.values())
-    d2h = sum(x.numel() * x.element_size() for x in h_out)
-    e_steps = max(1, min(args.steps, 5))
+    h_in = [pin(x).copy_(x) for x in (q, k, v, do)]
+    outs = outs_main if full else (oh, dqh, dkh, dvh)
+    h_out = [[pin(x) for x in outs] for _ in range(2)]
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    d2h = sum(x.numel() * x.element_size() for x in h_out[0])
+    e_steps = max(2, min(args.steps, 6))
+    sets_in = [(q, k, v, do), tuple(torch.empty_like(x) for x in (q, k, v, do))]
+    # a second output set only where the results are written in the seq layout
+    sets_out = [outs_main, tuple(torch.empty_like(x) for x in outs_main) if full else outs_main]
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(e_steps)]
+    ev_done = [torch.cuda.Event() for _ in range(e_steps)]
+    ev_out = [torch.cuda.Event() for _ in range(e_steps)]
+
+    def result_of(i):  # the device tensors step i's read-back copies
+        return sets_out[i % 2] if full else outs
+
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e_steps):
-        q.copy_(h_in["q"], non_blocking=True)
-        k.copy_(h_in["k"], non_blocking=True)
-        v.copy_(h_in["v"], non_blocking=True)
-        do.copy_(h_in["dout"], non_blocking=True)
-        step()
-        for hx, dx in zip(h_out, outs):
-            hx.copy_(dx, non_blocking=True)
+    up.wait_event(e0)
+    down.wait_event(e0)
+
+    def upload(i):
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(ev_done[i - 2])  # step i-2 has consumed this input set
+            for dx, hx in zip(sets_in[i % 2], h_in):
+                dx.copy_(hx, non_blocking=True)
+            ev_in[i].record(up)
+
+    def read_back(i):
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[i])
+            for hx, dx in zip(h_out[i % 2], result_of(i)):
+                hx.copy_(dx, non_blocking=True)
+            ev_out[i].record(down)
+
+    upload(0)
+    for i in range(e_steps):
+        if i + 1 < e_steps:
+            upload(i + 1)
+        stream.wait_event(ev_in[i])
+        if i >= 2:
+            stream.wait_event(ev_out[i - 2])  # step i-2's results are out of this output set
+        if not full and i >= 1:
+            stream.wait_event(ev_out[i - 1])  # one output set only
+        step(ins=sets_in[i % 2], outs_seq=sets_out[i % 2])
+        ev_done[i].record(stream)
+        read_back(i)
+    stream.wait_event(ev_out[e_steps - 1])
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e_steps
-    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dist, dev)
+    # the same work with no overlap: upload, step, read-back on one stream
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for i in range(e_steps):
+        for dx, hx in zip(sets_in[0], h_in):
+            dx.copy_(hx, non_blocking=True)
+        step(ins=sets_in[0], outs_seq=sets_out[0])
+        for hx, dx in zip(h_out[0], result_of(0)):
+            hx.copy_(dx, non_blocking=True)
+    s1.record(stream)
+    barrier()
+    e2e_serial_ms = max_over_ranks(s0.elapsed_time(s1) / e_steps, dist, dev)
+    st, site = uly.ulysses_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} at site {site:#x} in the end-to-end timing")
+    del sets_in, sets_out
 
     # ---- the sequence-parallel loss on the same tokens (Qwen3 vocabulary)
     loss = None
@@ -398,7 +461,11 @@ def run_ours(args, rank, world, dist):
                      "peak_source": f"{src} bf16 sustained (MEASURED_PEAKS.json)" if src == "measured"
                      else "fallback 1.7 PFLOP/s sustained"},
         "e2e": {"value": round(whole_job_throughput(world, step_flops, e2e_ms), 2), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+                "how": "pinned host buffers; per step an upload of the inputs and a read-back of the "
+                       "results, overlapped with the neighbouring steps' compute on two copy streams",
+                "steps": e_steps, "serial_ms_per_step": round(e2e_serial_ms, 3),
+                "serial_value": round(whole_job_throughput(world, step_flops, e2e_serial_ms), 2)},
         "fused_seq_layout_path": None if fused is None else {
             "what": "ulysses_attn_fwd_seq + ulysses_attn_bwd_seq: same step without the swap kernels",
             "ms_per_step": round(fused["ms_per_step"], 3),
