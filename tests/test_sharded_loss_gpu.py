@@ -41,7 +41,9 @@ def _oracle(logits, labels, P):
     (4, 2, 64, 1000, torch.float32),
     (2, 1, 96, 1001, torch.bfloat16),      # V not a multiple of 8: scalar path
     (8, 3, 64, 257, torch.float32),
-    (4, 1, 2048, 151936, torch.bfloat16),  # Qwen3 vocabulary
+    (4, 1, 2048, 151936, torch.bfloat16),  # Qwen3 vocabulary: with the gradient, rows held by clusters of 4
+    (4, 1, 128, 50000, torch.bfloat16),    # clusters of 2
+    (2, 1, 256, 151936, torch.float32),    # clusters of 8
 ])
 def test_sharded_ce_vs_oracle(uly, P, B, N, V, dtype):
     logits, labels = _case(P, B, N, V, dtype, seed=N + V)
