@@ -78,10 +78,11 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, log_dir: str = ""):
+        import tempfile
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        self.path = os.path.join(log_dir or tempfile.gettempdir(), f"clocks_rank{index}.csv")
 
     def __enter__(self):
         try:
@@ -213,7 +214,7 @@ def run_ours(args, rank, world, dist):
 
     # ---- timed region: device time, inputs resident in HBM
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev.index, args.clock_log_dir) as clk:
         barrier()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
@@ -559,6 +560,8 @@ def main():
                     help="override the workload's N (profiling smaller cases of the same kernels)")
     ap.add_argument("--oracle-rows", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log-dir", default="",
+                    help="directory for the raw nvidia-smi clock samples (default: the system temp dir)")
     ap.add_argument("--no-loss", action="store_true", help="skip the sequence-parallel loss measurement")
     ap.add_argument("--no-ring", action="store_true", help="skip the ring-attention measurement")
     ap.add_argument("--vocab", type=int, default=151936, help="vocabulary of the loss measurement (Qwen3)")
