@@ -12,9 +12,10 @@
 //   bwd_pre    : D_i and lse_i*log2(e) into fp32 scratch (padded rows get
 //                D = 0, lse = +inf so their probabilities are exactly 0).
 //   bwd_main   : one CTA per (shard*batch, KV head, 128-key tile).  K and V
-//                stay in shared memory; the CTA walks the G query heads of
-//                the group and every 128-row query tile that may attend to
-//                its keys.  dK and dV accumulate in TMEM across the whole
+//                stay in shared memory; the CTA walks every 128-row query
+//                tile that may attend to its keys, and for each of them the
+//                G query heads of the group back to back (their Q/dO rows
+//                are neighbours in memory).  dK and dV accumulate in TMEM across the whole
 //                group (no atomics); each dQ partial is added into an fp32
 //                accumulator with coalesced vector reductions.
 //   dq_convert : fp32 accumulator * scale -> bf16 dQ in the head layout.
@@ -254,8 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0;
             for (int it = 0; it < n_it && !*abort_flag; ++it) {
                 const int slot = it & 1;
-                const int h = kvh * p.G + it / n_m;
-                const int m = m_lo + it % n_m;
+                const int h = kvh * p.G + it % p.G;
+                const int m = m_lo + it / p.G;
                 if (!mbar_wait(&q_empty[slot], ((it >> 1) & 1) ^ 1, p.w, 0x51)) {
                     *abort_flag = 1;
                     break;
@@ -399,8 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t xq[32];
         float *dq_base = nullptr;
         auto read_dq = [&](int it) {
-            const int h = kvh * p.G + it / n_m;
-            const int m = m_lo + it % n_m;
+            const int h = kvh * p.G + it % p.G;
+            const int m = m_lo + it / p.G;
             tmem_ld32p(tdP + lane_off + c0, xq);
             tmem_ld_wait();
             tmem_ld_fence32p(xq);
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         for (int it = 0; it < n_it; ++it) {
             const int slot = it & 1;
-            const int64_t q0 = static_cast<int64_t>(m_lo + it % n_m) * kBM;
+            const int64_t q0 = static_cast<int64_t>(m_lo + it / p.G) * kBM;
             const float *lse_s = reinterpret_cast<const float *>(smem + BwdSmem::kLse + slot * 512) + c0;
             const float *D_s = reinterpret_cast<const float *>(smem + BwdSmem::kDv + slot * 512) + c0;
             reduce_groups(6, 7);  // of the partial read in the previous iteration
