@@ -14,13 +14,17 @@
 // instruction (load for seq->head, store for head->seq); a plain bulk copy
 // moves the contiguous side.  One elected thread per CTA keeps a ring of
 // shared-memory stages full, so every byte crosses HBM exactly once in each
-// direction in 16-byte-aligned bulk transfers.
+// direction in 16-byte-aligned bulk transfers.  Two CTAs share each SM (two
+// independent rings of 32 KB stages keep more transfers in flight than one
+// thread alone issues); rows too large for three stages in half the shared
+// memory run one CTA per SM instead.
 #include "uly_internal.h"
 
 namespace uly {
 namespace {
 
-constexpr int kSwapSmemBytes = 196608;  // ring of stages per CTA
+constexpr int kSwapSmemBytes = 196608;  // largest ring of stages per CTA
+constexpr int kSwapPairRing = 98304;     // ring when two CTAs share an SM
 constexpr int kSwapMaxStages = 8;
 
 __device__ __forceinline__ void tma_store_5d(const CUtensorMap *map, const void *smem_src, int c0, int c1, int c2,
@@ -131,9 +135,13 @@ __global__ void __launch_bounds__(32, 1) swap_kernel(const __grid_constant__ CUt
             tma_store_5d(&seq_map, buf, 0, 0, x.r, static_cast<int>(x.t0), x.s * static_cast<int>(p.B) + x.b);
         }
         bulk_commit();
-        // refill the stage released by the previous item's store
-        if (k >= 1 && issued < n_local) {
-            bulk_wait_read<1>();
+        // refill the stage released by the previous item's store; with a
+        // single stage, the one this item's store is still reading
+        if (issued < n_local && (k >= 1 || p.stages == 1)) {
+            if (p.stages == 1)
+                bulk_wait_read<0>();
+            else
+                bulk_wait_read<1>();
             issue_load(issued);
             ++issued;
         }
@@ -164,7 +172,10 @@ cudaError_t launch_swap(bool to_head, const void *src, void *dst, int64_t B, int
     if (T > Np)
         T = static_cast<int>(Np);
     const uint32_t stage_bytes = static_cast<uint32_t>(T * row_bytes);
-    int stages = static_cast<int>(kSwapSmemBytes / ((stage_bytes + 1023) & ~1023u));
+    const uint32_t stage_alloc = (stage_bytes + 1023) & ~1023u;
+    // two CTAs per SM with half the ring each, unless that leaves fewer than three stages
+    const bool pair = kSwapPairRing / stage_alloc >= 3;
+    int stages = static_cast<int>((pair ? kSwapPairRing : kSwapSmemBytes) / stage_alloc);
     if (stages > kSwapMaxStages)
         stages = kSwapMaxStages;
 
@@ -200,7 +211,7 @@ cudaError_t launch_swap(bool to_head, const void *src, void *dst, int64_t B, int
     p.w = wait_cfg();
 
     const size_t smem = static_cast<size_t>(stages) * ((stage_bytes + 1023) & ~1023u) + 1024;
-    int64_t grid = num_sms();
+    int64_t grid = (pair ? 2 : 1) * static_cast<int64_t>(num_sms());
     if (grid > p.nitems)
         grid = p.nitems;
     cudaError_t e;

@@ -19,6 +19,7 @@ pytestmark = pytest.mark.gpu
     (8, 1, 8 * 37, 8, 64),   # one head per rank, odd chunk
     (1, 1, 96, 4, 128),      # P = 1: the swap is the identity
     (4, 3, 4 * 300, 16, 64),
+    (2, 1, 8, 400, 128),     # 200 heads per shard: a 100 KB row (fp32) leaves the copy ring one stage
 ])
 def test_swap_bit_exact(uly, oracle_mod, dtype, P, B, N, H, d):
     g = torch.Generator().manual_seed(N + H)
