@@ -121,6 +121,36 @@ def _dev(*ts: torch.Tensor):
             raise ValueError("tensors must be contiguous")
 
 
+def _attn_args(q, k, v, like_q=(), like_k=(), lse=None, lse_shape=None, shards=None):
+    """The attention calls take every size from q and k; before any pointer
+    reaches the library, the other tensors must have the shapes and dtypes
+    include/ulysses.h states for them (a mismatch would be read or written
+    out of bounds)."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dim() != 5:
+            raise ValueError(f"{name} must be 5-D [shards][B][tokens][heads][d], got {tuple(t.shape)}")
+    if tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"v {tuple(v.shape)} must have the shape of k {tuple(k.shape)}")
+    if k.shape[:3] != q.shape[:3] or k.shape[4] != q.shape[4]:
+        raise ValueError(f"k {tuple(k.shape)} must match q {tuple(q.shape)} except in its head count")
+    if shards is not None and q.shape[0] != shards:
+        raise ValueError(f"the leading dimension of q must be P={shards}, got {q.shape[0]}")
+    for t in (k, v) + tuple(like_q) + tuple(like_k):
+        if t.dtype != q.dtype:
+            raise ValueError(f"all attention tensors must share q's dtype {q.dtype}, got {t.dtype}")
+    for t in like_q:
+        if tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"expected a tensor of q's shape {tuple(q.shape)}, got {tuple(t.shape)}")
+    for t in like_k:
+        if tuple(t.shape) != tuple(k.shape):
+            raise ValueError(f"expected a tensor of k's shape {tuple(k.shape)}, got {tuple(t.shape)}")
+    if lse is not None:
+        if lse.dtype != torch.float32:
+            raise ValueError(f"lse must be float32, got {lse.dtype}")
+        if tuple(lse.shape) != tuple(lse_shape):
+            raise ValueError(f"lse must have shape {tuple(lse_shape)}, got {tuple(lse.shape)}")
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -180,6 +210,7 @@ def _workspace(workspace, nbytes: int, device) -> torch.Tensor:
 def ulysses_attn_fwd(q, k, v, o, lse, causal: bool = True, cu_seqlens: Optional[Sequence[int]] = None,
                      softmax_scale: float = 0.0, workspace: Optional[torch.Tensor] = None, stream=None):
     """Attention forward over head shards; writes o and lse (see include/ulysses.h)."""
+    _attn_args(q, k, v, like_q=(o,), lse=lse, lse_shape=(q.shape[0], q.shape[1], q.shape[3], q.shape[2]))
     _dev(q, k, v, o, lse)
     S, B, N, Hq, d = q.shape
     Hkv = k.shape[3]
@@ -197,6 +228,8 @@ def ulysses_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = True,
                      cu_seqlens: Optional[Sequence[int]] = None, softmax_scale: float = 0.0,
                      workspace: Optional[torch.Tensor] = None, stream=None):
     """Attention backward; writes dq, dk, dv (see include/ulysses.h)."""
+    _attn_args(q, k, v, like_q=(o, dout, dq), like_k=(dk, dv), lse=lse,
+               lse_shape=(q.shape[0], q.shape[1], q.shape[3], q.shape[2]))
     _dev(q, k, v, o, lse, dout, dq, dk, dv)
     S, B, N, Hq, d = q.shape
     Hkv = k.shape[3]
@@ -215,6 +248,8 @@ def ulysses_attn_fwd_seq(q_seq, k_seq, v_seq, o_seq, lse, P: int, causal: bool =
                          workspace: Optional[torch.Tensor] = None, stream=None):
     """Attention over all P head shards read from and written to the
     sequence-sharded layout [P][B][N/P][H][d] (no swaps); lse [P][B][Hq/P][N]."""
+    _attn_args(q_seq, k_seq, v_seq, like_q=(o_seq,), lse=lse, shards=P,
+               lse_shape=(P, q_seq.shape[1], q_seq.shape[3] // max(P, 1), q_seq.shape[2] * P))
     _dev(q_seq, k_seq, v_seq, o_seq, lse)
     Ps, B, Np, Hq, d = q_seq.shape
     Hkv = k_seq.shape[3]
@@ -233,6 +268,8 @@ def ulysses_attn_bwd_seq(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_s
                          causal: bool = True, cu_seqlens: Optional[Sequence[int]] = None,
                          softmax_scale: float = 0.0, workspace: Optional[torch.Tensor] = None, stream=None):
     """Backward of ulysses_attn_fwd_seq, all tensors in the sequence-sharded layout."""
+    _attn_args(q_seq, k_seq, v_seq, like_q=(o_seq, dout_seq, dq_seq), like_k=(dk_seq, dv_seq), lse=lse,
+               shards=P, lse_shape=(P, q_seq.shape[1], q_seq.shape[3] // max(P, 1), q_seq.shape[2] * P))
     _dev(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_seq, dv_seq)
     Ps, B, Np, Hq, d = q_seq.shape
     Hkv = k_seq.shape[3]
@@ -254,6 +291,8 @@ def ulysses_attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = T
     """Attention backward without a workspace, for callers that cannot
     allocate device memory; its scratch is a fixed 64 MiB array inside the
     library (see include/ulysses.h for the limits and the ordering rule)."""
+    _attn_args(q, k, v, like_q=(o, dout, dq), like_k=(dk, dv), lse=lse,
+               lse_shape=(q.shape[0], q.shape[1], q.shape[3], q.shape[2]))
     _dev(q, k, v, o, lse, dout, dq, dk, dv)
     S, B, N, Hq, d = q.shape
     Hkv = k.shape[3]
@@ -270,6 +309,8 @@ def ulysses_attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = T
 def ulysses_ring_attn_fwd(q_seq, k_seq, v_seq, o_seq, lse, P: int, causal: bool = True,
                           softmax_scale: float = 0.0, workspace: Optional[torch.Tensor] = None, stream=None):
     """Ring attention over P chunks of the sequence-sharded layout; lse [P][B][Hq][N/P]."""
+    _attn_args(q_seq, k_seq, v_seq, like_q=(o_seq,), lse=lse, shards=P,
+               lse_shape=(P, q_seq.shape[1], q_seq.shape[3], q_seq.shape[2]))
     _dev(q_seq, k_seq, v_seq, o_seq, lse)
     Ps, B, Np, Hq, d = q_seq.shape
     Hkv = k_seq.shape[3]
@@ -287,6 +328,8 @@ def ulysses_ring_attn_bwd(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_
                           causal: bool = True, softmax_scale: float = 0.0,
                           workspace: Optional[torch.Tensor] = None, stream=None):
     """Backward of ulysses_ring_attn_fwd (final o and lse)."""
+    _attn_args(q_seq, k_seq, v_seq, like_q=(o_seq, dout_seq, dq_seq), like_k=(dk_seq, dv_seq), lse=lse,
+               shards=P, lse_shape=(P, q_seq.shape[1], q_seq.shape[3], q_seq.shape[2]))
     _dev(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_seq, dv_seq)
     Ps, B, Np, Hq, d = q_seq.shape
     Hkv = k_seq.shape[3]
