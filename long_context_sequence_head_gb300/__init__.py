@@ -354,6 +354,10 @@ def ulysses_sharded_ce_loss(logits, labels, P: int, dlogits: Optional[torch.Tens
     -100 = ignored).  Returns (shard_loss [P] fp32, shard_good [P] int64,
     total [1] fp32) on the device; fills dlogits (like logits) if given.
     """
+    if logits.dim() != 4 or logits.shape[0] != P:
+        raise ValueError(f"logits must be [P={P}][B][N/P][V], got {tuple(logits.shape)}")
+    if dlogits is not None and (tuple(dlogits.shape) != tuple(logits.shape) or dlogits.dtype != logits.dtype):
+        raise ValueError("dlogits must have the shape and dtype of logits")
     _dev(logits, labels)
     if dlogits is not None:
         _dev(dlogits)

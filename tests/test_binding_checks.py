@@ -67,3 +67,17 @@ def test_seq_and_ring_layouts():
         uly.ulysses_ring_attn_fwd(q, k, v, o, lse_seq, P)
     with pytest.raises(ValueError, match="leading dimension"):
         uly.ulysses_attn_fwd_seq(q, k, v, o, lse_seq, 4)
+
+
+def test_sharded_loss_arguments():
+    P, Np, V = 2, 8, 64
+    logits = _t(P, B, Np, V)
+    labels = torch.zeros(P, B, Np, dtype=torch.int64)
+    with pytest.raises(ValueError, match="CUDA device"):
+        uly.ulysses_sharded_ce_loss(logits, labels, P, dlogits=_t(P, B, Np, V))
+    with pytest.raises(ValueError, match="shape and dtype of logits"):
+        uly.ulysses_sharded_ce_loss(logits, labels, P, dlogits=_t(P, B, Np, V - 8))
+    with pytest.raises(ValueError, match="shape and dtype of logits"):
+        uly.ulysses_sharded_ce_loss(logits, labels, P, dlogits=_t(P, B, Np, V, dtype=torch.float32))
+    with pytest.raises(ValueError, match="logits must be"):
+        uly.ulysses_sharded_ce_loss(logits, labels, 4)
