@@ -408,8 +408,9 @@ def run_ours(args, rank, world, dist):
                 "tokens": B * N, "vocab": V, "dtype": "bf16", "ms": round(loss_ms, 3),
                 "algorithmic_bytes": alg, "gbps": round(alg / (loss_ms * 1e-3) / 1e9, 1),
                 "frac_of_hbm": round(alg / (loss_ms * 1e-3) / 1e9 / _peaks()[0], 3),
-                "note": "with the gradient each row is held on chip by a cluster of CTAs (4 for this "
-                        "vocabulary): one HBM read and one write per logit, the algorithmic bytes"}
+                "note": "with the gradient each row is held on chip by a cluster of 1, 2, 4 or 8 CTAs "
+                        "(by vocabulary size; 4 for 151936 in bf16): one HBM read and one write per "
+                        "logit, the algorithmic bytes"}
         del logits, labels, dlogits, ws_l
         torch.cuda.empty_cache()
 
