@@ -142,28 +142,47 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *__restrict
 }
 
 // ---------------------------------------------------------- dq convert
+// One block per 32-row slab of one (sb, h, 128-row tile).  In the accumulator
+// each of the slab's 32 column groups is 32 rows x 16 B = 512 contiguous bytes;
+// the slab is staged through shared memory and written as whole bf16 rows, so
+// both the reads and the writes are contiguous runs.
+constexpr int kCvtRows = 32;
+constexpr int kCvtPitch = kD + 4;  // floats per staged row; +4 spreads the group stores over all banks
+
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc, uint16_t *__restrict__ dq,
                                                          int64_t SB, int64_t N, int64_t Npad, int Hq, float scale,
                                                          RowLayout L)
 {
-    // thread -> (sb, h, row, group of 4 columns); lanes vary the group so the
-    // bf16 row writes are contiguous
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t total = SB * Hq * N * 32;
-    if (t >= total)
-        return;
-    const int g = static_cast<int>(t & 31);
-    int64_t rest = t >> 5;
-    const int64_t i = rest % N;
-    rest /= N;
+    __shared__ __align__(16) float tile[kCvtRows * kCvtPitch];
+    const int64_t ntiles = Npad / kBM;
+    int64_t rest = blockIdx.x;
+    const int slab = static_cast<int>(rest % (kBM / kCvtRows));
+    rest /= kBM / kCvtRows;
+    const int64_t mt = rest % ntiles;
+    rest /= ntiles;
     const int h = static_cast<int>(rest % Hq);
     const int64_t sb = rest / Hq;
-    const float4 v = *reinterpret_cast<const float4 *>(
-        acc + (((sb * Hq + h) * (Npad / kBM) + i / kBM) * 32 + g) * (kBM * 4) + (i % kBM) * 4);
-    uint2 out;
-    out.x = pack_bf16x2(v.x * scale, v.y * scale);
-    out.y = pack_bf16x2(v.z * scale, v.w * scale);
-    *reinterpret_cast<uint2 *>(dq + L.off(N, sb, i, Hq, h, kD) + g * 4) = out;
+    const float *src = acc + ((sb * Hq + h) * ntiles + mt) * (32 * kBM * 4);
+    const int r0 = slab * kCvtRows;
+    // consecutive threads take consecutive rows of one column group
+    for (int k = threadIdx.x; k < 32 * kCvtRows; k += 256) {
+        const int g = k / kCvtRows, r = k % kCvtRows;
+        *reinterpret_cast<float4 *>(tile + r * kCvtPitch + g * 4) =
+            *reinterpret_cast<const float4 *>(src + (g * kBM + r0 + r) * 4);
+    }
+    __syncthreads();
+    // a warp writes whole rows: lane l holds columns 4l .. 4l+3
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int r = w; r < kCvtRows; r += 8) {
+        const int64_t i = mt * kBM + r0 + r;
+        if (i >= N)
+            break;
+        const float4 v = *reinterpret_cast<const float4 *>(tile + r * kCvtPitch + lane * 4);
+        uint2 out;
+        out.x = pack_bf16x2(v.x * scale, v.y * scale);
+        out.y = pack_bf16x2(v.z * scale, v.w * scale);
+        *reinterpret_cast<uint2 *>(dq + L.off(N, sb, i, Hq, h, kD) + lane * 4) = out;
+    }
 }
 
 // ----------------------------------------------------------------- main
@@ -630,8 +649,8 @@ cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *
         return e;
     // 4. dQ = scale * accumulator -> bf16
     {
-        const int64_t total = s.SB * s.Hq * s.N * 32;
-        dq_convert_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
+        const int64_t blocks = s.SB * s.Hq * (Npad / kBM) * (kBM / kCvtRows);
+        dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
             scr.dq_acc, static_cast<uint16_t *>(dq), s.SB, s.N, Npad, s.Hq, s.scale, s.L);
     }
     return cudaGetLastError();
