@@ -102,42 +102,57 @@ __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x <
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
 // ------------------------------------------------------------------ pre
+// One warp per (shard*batch, token): the token's Hq rows of O and dO are
+// adjacent in both layouts (Hq x 256 contiguous bytes each), so the warp reads
+// them in 512-byte runs, two heads per pass (lanes 0-15 and 16-31, 16 bytes
+// a lane), and reduces each head's dot product within its half-warp.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *__restrict__ o,
                                                       const uint16_t *__restrict__ dout,
                                                       const float *__restrict__ lse, float *__restrict__ lse2,
                                                       float *__restrict__ Dv, int64_t SB, int64_t N, int64_t Npad,
                                                       int Hq, RowLayout L)
 {
-    // one warp per (sb, h, row); lane reads 4 bf16 of O and dO (8 bytes each)
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    const int64_t total = SB * Hq * Npad;
-    if (gw >= total)
+    const int lane = lane_id();
+    if (gw >= SB * Npad)
         return;
     const int64_t i = gw % Npad;
-    const int64_t sbh = gw / Npad;
-    const int h = static_cast<int>(sbh % Hq);
-    const int64_t sb = sbh / Hq;
+    const int64_t sb = gw / Npad;
     if (i >= N) {
-        if (lane == 0) {
-            Dv[gw] = 0.f;
-            lse2[gw] = INFINITY;
+        // padded rows: probabilities exactly 0 in the main kernel
+        for (int h = lane; h < Hq; h += 32) {
+            Dv[(sb * Hq + h) * Npad + i] = 0.f;
+            lse2[(sb * Hq + h) * Npad + i] = INFINITY;
         }
         return;
     }
-    const int64_t off = L.off(N, sb, i, Hq, h, kD) + lane * 4;
-    const uint2 a = *reinterpret_cast<const uint2 *>(o + off);
-    const uint2 b = *reinterpret_cast<const uint2 *>(dout + off);
-    float acc = bf16lo(a.x) * bf16lo(b.x);
-    acc = fmaf(bf16hi(a.x), bf16hi(b.x), acc);
-    acc = fmaf(bf16lo(a.y), bf16lo(b.y), acc);
-    acc = fmaf(bf16hi(a.y), bf16hi(b.y), acc);
+    const int64_t off = L.off(N, sb, i, Hq, 0, kD);
+    const uint4 *o4 = reinterpret_cast<const uint4 *>(o + off);
+    const uint4 *d4 = reinterpret_cast<const uint4 *>(dout + off);
+    const int n16 = Hq * (kD / 8);  // 16-byte pieces of the token's rows
+    for (int u0 = 0; u0 < n16; u0 += 32) {
+        const int u = u0 + lane;
+        float acc = 0.f;
+        if (u < n16) {
+            const uint4 a = o4[u], b = d4[u];
+            acc = bf16lo(a.x) * bf16lo(b.x);
+            acc = fmaf(bf16hi(a.x), bf16hi(b.x), acc);
+            acc = fmaf(bf16lo(a.y), bf16lo(b.y), acc);
+            acc = fmaf(bf16hi(a.y), bf16hi(b.y), acc);
+            acc = fmaf(bf16lo(a.z), bf16lo(b.z), acc);
+            acc = fmaf(bf16hi(a.z), bf16hi(b.z), acc);
+            acc = fmaf(bf16lo(a.w), bf16lo(b.w), acc);
+            acc = fmaf(bf16hi(a.w), bf16hi(b.w), acc);
+        }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1)
-        acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) {
-        Dv[gw] = acc;
-        lse2[gw] = lse[sbh * N + i] * 1.4426950408889634f;
+        for (int sft = 8; sft > 0; sft >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+        if (u < n16 && (lane & 15) == 0) {
+            const int h = u / (kD / 8);
+            const int64_t row = (sb * Hq + h) * Npad + i;
+            Dv[row] = acc;
+            lse2[row] = lse[(sb * Hq + h) * N + i] * 1.4426950408889634f;
+        }
     }
 }
 
@@ -604,7 +619,7 @@ cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *
     cudaError_t e;
     // 1. D, lse*log2(e); 2. zero the dQ accumulator
     {
-        const int64_t warps = s.SB * s.Hq * Npad;
+        const int64_t warps = s.SB * Npad;
         const int64_t blocks = (warps * 32 + 255) / 256;
         bwd_pre_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
             static_cast<const uint16_t *>(o), static_cast<const uint16_t *>(dout), lse, scr.lse2, scr.D, s.SB, s.N,
