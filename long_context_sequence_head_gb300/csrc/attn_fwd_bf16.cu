@@ -18,7 +18,10 @@
 // TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  P (bf16) is
 // written over the first 64 columns of S and fed to the PV product straight
 // from TMEM.  O is rescaled in TMEM only when the running row maximum grows by
-// more than 2^8 (lazy rescaling), so P stays below 256.
+// more than 2^8 (lazy rescaling), so P stays below 256.  A tile's exponentials
+// are first taken against the running maximum without computing the tile's
+// own maximum; their sum proves whether the lazy rule keeps that maximum, and
+// only when it may not (or on a row's first tile) is the tile redone exactly.
 #include "uly_internal.h"
 
 namespace uly {
@@ -298,55 +301,107 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (c < lo_c || c >= hi_c)
                             u[c] = __float_as_uint(-INFINITY);
                 }
-                // row maximum with 8 independent partial maxima (short chains)
-                float pm[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    pm[e] = __uint_as_float(u[e]);
-#pragma unroll
-                for (int c = 8; c < kBN; c += 8)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        pm[e] = fmaxf(pm[e], __uint_as_float(u[c + e]));
-                const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-                const float m_cand = mx * p.scale_log2;
-                float alpha = 1.f;
-                bool rescale = false;
-                if (m_cand > m + kRescaleThreshold) {
-                    alpha = ex2_approx(m - m_cand);
-                    rescale = (j > 0) && (m != -INFINITY);
-                    m = m_cand;
-                }
-                l *= alpha;
-                const float m_use = (m == -INFINITY) ? 0.f : m;
+                // Speculate that the running maximum m still holds: the tile's
+                // exponentials against m all stay <= 2^8 exactly when the lazy
+                // rescale rule would keep m, and their sum <= 2^8 proves it.  On
+                // a row's first tile, or when the sum says the maximum may have
+                // grown, the tile is redone exactly from S, still in TMEM.
                 const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
-                const float2 nm2 = make_float2(-m_use, -m_use);
                 float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
-                // p = 2^(s * scale * log2(e) - m) on the SFU (masked scores are
-                // -inf and give exactly 0); the scale-and-shift and the row sum
-                // run as packed f32x2 pairs, the sum in four independent chains
+                const bool first = __any_sync(0xffffffffu, m == -INFINITY);
+                if (!first) {
+                    const float2 nm2 = make_float2(-m, -m);
 #pragma unroll
-                for (int c = 0; c < kBN; c += 2) {
-                    const float2 x = ffma2(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2, nm2);
-                    const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                    rs2[(c >> 1) & 3] = fadd2(rs2[(c >> 1) & 3], pv);
-                    u[c] = __float_as_uint(pv.x);
-                    u[c + 1] = __float_as_uint(pv.y);
+                    for (int c = 0; c < kBN; c += 2) {
+                        const float2 x = ffma2(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2, nm2);
+                        const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        rs2[(c >> 1) & 3] = fadd2(rs2[(c >> 1) & 3], pv);
+                        u[c] = __float_as_uint(pv.x);
+                        u[c + 1] = __float_as_uint(pv.y);
+                    }
                 }
-                const float2 r01 = fadd2(rs2[0], rs2[1]), r23 = fadd2(rs2[2], rs2[3]);
-                const float2 r = fadd2(r01, r23);
-                l += r.x + r.y;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        pk[c] = pack_bf16x2(__uint_as_float(u[half * 64 + 2 * c]),
-                                            __uint_as_float(u[half * 64 + 2 * c + 1]));
-                    tmem_st32p(tS + half * 32, pk);
+                float rsum;
+                {
+                    const float2 r01 = fadd2(rs2[0], rs2[1]), r23 = fadd2(rs2[2], rs2[3]);
+                    const float2 r = fadd2(r01, r23);
+                    rsum = r.x + r.y;
                 }
+                float alpha = 1.f;
+                bool rescale = false;
+                if (first || __any_sync(0xffffffffu, !(rsum <= 256.f))) {
+                    // exact: row maximum of S, then the exponentials, 64 columns at a time
+                    float pm[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        pm[e] = -INFINITY;
+                    const int lo_c = masked ? static_cast<int>(max(lo - key0, int64_t(0))) : 0;
+                    const int hi_c = masked ? static_cast<int>(min(hi - key0, int64_t(kBN))) : kBN;
+#pragma unroll 1
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t v[64];
+                        tmem_ld32p(tS + half * 64, v);
+                        tmem_ld32p(tS + half * 64 + 32, v + 32);
+                        tmem_ld_wait();
+                        tmem_ld_fence32p(v);
+                        tmem_ld_fence32p(v + 32);
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            const int cg = half * 64 + c;
+                            const float sv = (cg < lo_c || cg >= hi_c) ? -INFINITY : __uint_as_float(v[c]);
+                            pm[c & 7] = fmaxf(pm[c & 7], sv);
+                        }
+                    }
+                    const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                           fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+                    const float m_cand = mx * p.scale_log2;
+                    if (m_cand > m + kRescaleThreshold) {
+                        alpha = ex2_approx(m - m_cand);
+                        rescale = (j > 0) && (m != -INFINITY);
+                        m = m_cand;
+                    }
+                    const float m_use = (m == -INFINITY) ? 0.f : m;
+                    const float2 nm2 = make_float2(-m_use, -m_use);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        rs2[e] = make_float2(0.f, 0.f);
+#pragma unroll 1
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t v[64];
+                        tmem_ld32p(tS + half * 64, v);
+                        tmem_ld32p(tS + half * 64 + 32, v + 32);
+                        tmem_ld_wait();
+                        tmem_ld_fence32p(v);
+                        tmem_ld_fence32p(v + 32);
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int c = 0; c < 64; c += 2) {
+                            const int cg = half * 64 + c;
+                            const float s0 = (cg < lo_c || cg >= hi_c) ? -INFINITY : __uint_as_float(v[c]);
+                            const float s1 = (cg + 1 < lo_c || cg + 1 >= hi_c) ? -INFINITY : __uint_as_float(v[c + 1]);
+                            const float2 x = ffma2(make_float2(s0, s1), sl2, nm2);
+                            const float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                            rs2[(c >> 1) & 3] = fadd2(rs2[(c >> 1) & 3], pv);
+                            pk[c >> 1] = pack_bf16x2(pv.x, pv.y);
+                        }
+                        // P of S columns half*64.. lands on S columns this thread has read
+                        tmem_st32p(tS + half * 32, pk);
+                    }
+                    const float2 r01 = fadd2(rs2[0], rs2[1]), r23 = fadd2(rs2[2], rs2[3]);
+                    const float2 r = fadd2(r01, r23);
+                    rsum = r.x + r.y;
+                } else {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            pk[c] = pack_bf16x2(__uint_as_float(u[half * 64 + 2 * c]),
+                                                __uint_as_float(u[half * 64 + 2 * c + 1]));
+                        tmem_st32p(tS + half * 32, pk);
+                    }
+                }
+                l = l * alpha + rsum;
                 if (__any_sync(0xffffffffu, rescale)) {
                     const float a = rescale ? alpha : 1.f;
 #pragma unroll
