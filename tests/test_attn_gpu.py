@@ -99,7 +99,9 @@ def _ramp_inputs(N, Hq, Hkv, d, seed, kind):
                row, so the running maximum keeps jumping by more than the
                forward's 2^8 rescale threshold;
       "fall":  the mirror image, the first key tile holds the maximum;
-      "spike": a_j = 0 except two late keys with scores ~40."""
+      "spike": a_j = 0 except two late keys with scores ~40;
+      "stairs": a_j constant over each 128-key tile, at levels (log2 units)
+               0, 4, 14, 15, 19, 29, 30, 31: see test_running_max_speculation."""
     g = torch.Generator().manual_seed(seed)
     u = torch.randn(d, generator=g, dtype=torch.float64)
     u /= u.norm()
@@ -108,6 +110,10 @@ def _ramp_inputs(N, Hq, Hkv, d, seed, kind):
         a = 57.0 * t
     elif kind == "fall":
         a = 57.0 * (1.0 - t)
+    elif kind == "stairs":
+        levels = torch.tensor([0.0, 4.0, 14.0, 15.0, 19.0, 29.0, 30.0, 31.0], dtype=torch.float64)
+        # s = 8 a / sqrt(d) natural-log units = level log2 units
+        a = (levels * math.log(2.0) * math.sqrt(d) / 8.0).repeat_interleave(128)[:N]
     else:
         a = torch.zeros(N, dtype=torch.float64)
         a[int(0.7 * N)] = a[int(0.9 * N)] = 40.0 * math.sqrt(d) / 8.0
@@ -189,6 +195,53 @@ def test_score_ramps_exercise_the_rescale(uly, kind, causal):
     # than the plain bound) -- see _dq_bf16_operand_error.
     floor = _dq_bf16_operand_error(q, k, v, do, causal)
     _attn_inputs_case(uly, q, k, v, do, causal, None, label=f" ramp-{kind}",
+                      tol={"dq": max(REL_TOL["bf16"], 2.0 * floor)})
+
+
+def _speculation_paths(q, k, causal, tile=128):
+    """Per (row, key tile) after a row's first tile, which way the forward's
+    running-maximum speculation goes (query head 0, log2 units): "kept" when
+    the tile's exponentials against the running maximum m sum to at most 2^8;
+    otherwise the tile is redone exactly, "grow" if its maximum exceeds m + 8
+    (m moves, O is rescaled) and "redo" if not (m stays)."""
+    d = q.shape[-1]
+    s = (q[0, 0, :, 0].double() @ k[0, 0, :, 0].double().T) * (1.0 / math.sqrt(d)) / math.log(2.0)
+    N = s.shape[0]
+    if causal:
+        s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), -math.inf)
+    counts = {"kept": 0, "redo": 0, "grow": 0}
+    for i in range(N):
+        m = -math.inf
+        for c in range(0, N, tile):
+            x = s[i, c:c + tile]
+            mx = float(x.max())
+            if mx == -math.inf and m == -math.inf:
+                continue
+            if m == -math.inf:
+                m = mx
+            elif float(torch.exp2(x - m).sum()) <= 256.0:
+                counts["kept"] += 1
+            elif mx > m + 8.0:
+                counts["grow"] += 1
+                m = mx
+            else:
+                counts["redo"] += 1
+    return counts
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_running_max_speculation(uly, causal):
+    """Key tiles at stepped score levels drive every branch of the forward's
+    speculative running maximum: tiles kept on the speculation, tiles redone
+    with the maximum unchanged (their exponentials sum above 2^8 while none
+    lies more than 8 above the running maximum in log2 units) and tiles where
+    the maximum moves and O is rescaled.  Results against the oracle."""
+    N, Hq, Hkv, d = 1024, 4, 2, 128
+    q, k, v, do = _ramp_inputs(N, Hq, Hkv, d, seed=37, kind="stairs")
+    paths = _speculation_paths(q, k, causal)
+    assert all(n >= 100 for n in paths.values()), paths
+    floor = _dq_bf16_operand_error(q, k, v, do, causal)
+    _attn_inputs_case(uly, q, k, v, do, causal, None, label=" stairs",
                       tol={"dq": max(REL_TOL["bf16"], 2.0 * floor)})
 
 
