@@ -171,9 +171,10 @@ def run_ours(args, rank, world, dist):
     q_in, k_in, v_in, do_in = q, k, v, do
     outs_main = (o_seq, dq_seq, dk_seq, dv_seq)
 
-    def step(ev=None, ins=None, outs_seq=None):
+    def step(ev=None, ins=None, outs_seq=None, after_o=None, before_do=None):
         """One layer step on the inputs `ins` = (q, k, v, dO) in the seq layout,
-        writing (O, dQ, dK, dV) in the seq layout to `outs_seq`."""
+        writing (O, dQ, dK, dV) in the seq layout to `outs_seq`.  `after_o` is
+        called once O is final, `before_do` before dO is first read."""
         q, k, v, do = ins if ins is not None else (q_in, k_in, v_in, do_in)
         o_seq, dq_seq, dk_seq, dv_seq = outs_seq if outs_seq is not None else outs_main
 
@@ -189,6 +190,10 @@ def run_ours(args, rank, world, dist):
         mark(2)
         if full:
             uly.ulysses_head_to_seq(oh, o_seq, P)
+        if after_o is not None:
+            after_o()
+        if before_do is not None:
+            before_do()
         uly.ulysses_seq_to_head(do, doh, P)
         mark(3)
         uly.ulysses_attn_bwd(qh[:S], kh[:S], vh[:S], oh, lse, doh[:S], dqh, dkh, dvh, causal=w.causal,
@@ -299,20 +304,24 @@ def run_ours(args, rank, world, dist):
     # its O, dQ, dK, dV back.  Served as a stream of batches: two sets of device
     # buffers, the upload of step i+1 (one copy stream) and the read-back of
     # step i-1 (another) run while step i computes; the timed region opens
-    # before the first upload and closes after the last read-back.  The same
-    # loop on one stream (no overlap) is reported beside it.
+    # before the first upload and closes after the last read-back.  A step
+    # starts once its Q, K, V are in (dO is first read after the forward) and
+    # its O is read back while its backward runs.  The same loop on one stream
+    # (no overlap) is reported beside it.
     pin = lambda x: torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     h_in = [pin(x).copy_(x) for x in (q, k, v, do)]
     outs = outs_main if full else (oh, dqh, dkh, dvh)
     h_out = [[pin(x) for x in outs] for _ in range(2)]
     h2d = sum(x.numel() * x.element_size() for x in h_in)
     d2h = sum(x.numel() * x.element_size() for x in h_out[0])
-    e_steps = max(2, min(args.steps, 6))
+    e_steps = max(2, args.steps)
     sets_in = [(q, k, v, do), tuple(torch.empty_like(x) for x in (q, k, v, do))]
     # a second output set only where the results are written in the seq layout
     sets_out = [outs_main, tuple(torch.empty_like(x) for x in outs_main) if full else outs_main]
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(e_steps)]
+    ev_do = [torch.cuda.Event() for _ in range(e_steps)]
+    ev_o = [torch.cuda.Event() for _ in range(e_steps)]
     ev_done = [torch.cuda.Event() for _ in range(e_steps)]
     ev_out = [torch.cuda.Event() for _ in range(e_steps)]
 
@@ -330,14 +339,22 @@ def run_ours(args, rank, world, dist):
         with torch.cuda.stream(up):
             if i >= 2:
                 up.wait_event(ev_done[i - 2])  # step i-2 has consumed this input set
-            for dx, hx in zip(sets_in[i % 2], h_in):
+            for dx, hx in zip(sets_in[i % 2][:3], h_in[:3]):
                 dx.copy_(hx, non_blocking=True)
-            ev_in[i].record(up)
+            ev_in[i].record(up)  # Q, K, V
+            sets_in[i % 2][3].copy_(h_in[3], non_blocking=True)
+            ev_do[i].record(up)
+
+    def read_back_o(i):
+        ev_o[i].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_o[i])
+            h_out[i % 2][0].copy_(result_of(i)[0], non_blocking=True)
 
     def read_back(i):
         with torch.cuda.stream(down):
             down.wait_event(ev_done[i])
-            for hx, dx in zip(h_out[i % 2], result_of(i)):
+            for hx, dx in zip(h_out[i % 2][1:], result_of(i)[1:]):
                 hx.copy_(dx, non_blocking=True)
             ev_out[i].record(down)
 
@@ -350,7 +367,8 @@ def run_ours(args, rank, world, dist):
             stream.wait_event(ev_out[i - 2])  # step i-2's results are out of this output set
         if not full and i >= 1:
             stream.wait_event(ev_out[i - 1])  # one output set only
-        step(ins=sets_in[i % 2], outs_seq=sets_out[i % 2])
+        step(ins=sets_in[i % 2], outs_seq=sets_out[i % 2], after_o=lambda: read_back_o(i),
+             before_do=lambda: stream.wait_event(ev_do[i]))
         ev_done[i].record(stream)
         read_back(i)
     stream.wait_event(ev_out[e_steps - 1])
@@ -465,7 +483,8 @@ def run_ours(args, rank, world, dist):
         "e2e": {"value": round(whole_job_throughput(world, step_flops, e2e_ms), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
                 "how": "pinned host buffers; per step an upload of the inputs and a read-back of the "
-                       "results, overlapped with the neighbouring steps' compute on two copy streams",
+                       "results, overlapped with the neighbouring steps' compute on two copy streams; "
+                       "a step starts once its Q, K, V are in and its O is read back during its backward",
                 "steps": e_steps, "serial_ms_per_step": round(e2e_serial_ms, 3),
                 "serial_value": round(whole_job_throughput(world, step_flops, e2e_serial_ms), 2)},
         "fused_seq_layout_path": None if fused is None else {
