@@ -61,6 +61,7 @@ struct BwdSmem {
 struct BwdParams {
     int64_t SB, N, Npad;
     int Hq, Hkv, G, n_ktiles;
+    int group;  // problems interleaved in the grid
     int causal;
     const int32_t *cu;
     int num_docs;
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
 }
 
 // ----------------------------------------------------------------- main
+template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -237,9 +239,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- work unit: problem-major (all resident CTAs share one (shard*batch,
     // KV head) problem, so its Q/dO tiles and dQ accumulator stay in L2), key
-    // tiles with the most query tiles first within a problem ----
-    const int n_blk = static_cast<int>(blockIdx.x % p.n_ktiles);
-    const int prob = static_cast<int>(blockIdx.x / p.n_ktiles);
+    // tiles with the most query tiles first within a problem.  Where one key
+    // tile's walk is long next to a problem's share of the GPU (short
+    // sequences, documents), the last problem's longest walks would run on
+    // alone at the end; there groups of problems interleave their key tiles
+    // instead (the launcher picks the group size) ----
+    int n_blk, prob;
+    if constexpr (!kGrouped) {
+        n_blk = static_cast<int>(blockIdx.x % p.n_ktiles);
+        prob = static_cast<int>(blockIdx.x / p.n_ktiles);
+    } else {
+        // groups of p.group problems, key tiles interleaved across the group
+        const int64_t nprob = p.SB * p.Hkv;
+        const int64_t grp = blockIdx.x / (static_cast<int64_t>(p.group) * p.n_ktiles);
+        const int64_t rem = blockIdx.x % (static_cast<int64_t>(p.group) * p.n_ktiles);
+        const int64_t gsize = (nprob - grp * p.group < p.group) ? nprob - grp * p.group : p.group;
+        n_blk = static_cast<int>(rem / gsize);
+        prob = static_cast<int>(grp * p.group + rem % gsize);
+    }
     const int kvh = prob % p.Hkv;
     const int sb = prob / p.Hkv;
     const int64_t kv0 = static_cast<int64_t>(n_blk) * kBN;
@@ -652,13 +669,30 @@ cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *
     p.dv = static_cast<uint16_t *>(dv);
     p.w = wait_cfg();
     p.L = s.L;
+    {
+        int64_t work = 0, longest = 0;
+        for (int n = 0; n < p.n_ktiles; ++n) {
+            const int64_t kv0 = static_cast<int64_t>(n) * kBN;
+            const int64_t key_last = (kv0 + kBN - 1 < s.N - 1) ? kv0 + kBN - 1 : s.N - 1;
+            int64_t row_lo, row_hi, t0, t1;
+            doc_range_host(s.cu_host, s.num_docs, s.N, kv0, row_lo, t0);
+            doc_range_host(s.cu_host, s.num_docs, s.N, key_last, t1, row_hi);
+            if (s.causal)
+                row_lo = kv0;
+            const int64_t n_it = static_cast<int64_t>(p.G) * ((row_hi - 1) / kBM - row_lo / kBM + 1);
+            work += n_it;
+            longest = n_it > longest ? n_it : longest;
+        }
+        p.group = group_for(work, longest, s.SB * s.Hkv);
+    }
     const size_t smem = BwdSmem::kTotal;
-    e = cudaFuncSetAttribute(attn_bwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kernel = p.group > 1 ? attn_bwd_bf16_kernel<true> : attn_bwd_bf16_kernel<false>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
     const int64_t units = s.SB * s.Hkv * p.n_ktiles;
-    attn_bwd_bf16_kernel<<<static_cast<unsigned>(units), kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+    kernel<<<static_cast<unsigned>(units), kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;

@@ -18,6 +18,38 @@ unsigned *device_status_ptr();
 uint64_t wait_limit_ns();
 int num_sms();
 
+// Rows [lo, hi) of the document holding token i (the whole sequence without documents).
+inline void doc_range_host(const int32_t *cu, int num_docs, int64_t N, int64_t i, int64_t &lo, int64_t &hi)
+{
+    lo = 0;
+    hi = N;
+    if (cu == nullptr || num_docs <= 0)
+        return;
+    int a = 0, b = num_docs;
+    while (b - a > 1) {
+        const int m = (a + b) >> 1;
+        if (static_cast<int64_t>(cu[m]) <= i)
+            a = m;
+        else
+            b = m;
+    }
+    lo = cu[a];
+    hi = cu[a + 1];
+}
+
+// Problems interleaved per group of the grid: the fewest that make a group's
+// work per SM at least 1.5 times the longest single work unit, so that the
+// last group's longest units do not run on alone at the end of the launch.
+inline int group_for(int64_t work_per_problem, int64_t longest_unit, int64_t nprob)
+{
+    if (work_per_problem <= 0)
+        return 1;
+    int64_t g = (3 * longest_unit * num_sms() + 2 * work_per_problem - 1) / (2 * work_per_problem);
+    if (g > nprob)
+        g = nprob;
+    return g < 1 ? 1 : static_cast<int>(g);
+}
+
 inline WaitCfg wait_cfg() { return WaitCfg{device_status_ptr(), wait_limit_ns()}; }
 
 // ---------------------------------------------------------------- swap
@@ -70,6 +102,7 @@ struct AttnShape {
     int Hq, Hkv, d;  // per shard
     int causal;
     const int32_t *cu_dev;  // device cu_seqlens [num_docs+1] or nullptr
+    const int32_t *cu_host; // the same on the host (valid during the call) or nullptr
     int num_docs;
     float scale;      // softmax scale
     RowLayout L;     // where q/k/v/o/dout/dq/dk/dv rows live

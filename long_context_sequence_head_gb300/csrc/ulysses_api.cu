@@ -275,6 +275,7 @@ uly_status attn_fwd_impl(const void *q, const void *k, const void *v, void *o, f
     sh.causal = causal;
     sh.num_docs = cu_seqlens_host ? num_docs : 0;
     sh.cu_dev = nullptr;
+    sh.cu_host = cu_seqlens_host;
     sh.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
     sh.L = L;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -322,6 +323,7 @@ uly_status attn_bwd_impl(const void *q, const void *k, const void *v, const void
     sh.causal = causal;
     sh.num_docs = cu_seqlens_host ? num_docs : 0;
     sh.cu_dev = nullptr;
+    sh.cu_host = cu_seqlens_host;
     sh.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
     sh.L = L;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
