@@ -261,7 +261,12 @@ def run_ours(args, rank, world, dist):
 
     # ---- ring attention on the same inputs (chunks of the seq layout, all heads)
     ring = None
-    if full and not args.no_ring:
+    ring_skipped = None
+    if w.packed_docs and full and not args.no_ring:
+        # the ring path computes plain causal / non-causal attention: timing it on
+        # this workload would time a different (larger) computation
+        ring_skipped = "ring attention takes no document mask; not timed on a packed-document workload"
+    if full and not args.no_ring and not w.packed_docs:
         Np = N // P
         lse_r = torch.empty(P, B, w.Hq, Np, dtype=torch.float32, device=dev)
         ws_rf = torch.empty(uly.load().ulysses_ring_attn_workspace_size(B, N, w.Hq, w.Hkv, d, P, 0,
@@ -492,7 +497,7 @@ def run_ours(args, rank, world, dist):
             "ms_per_step": round(fused["ms_per_step"], 3),
             "value": round(whole_job_throughput(world, step_flops, fused["ms_per_step"]), 2), "unit": UNIT,
             "tokens_per_s": round(world * B * N / (fused["ms_per_step"] * 1e-3), 1)},
-        "ring_attention": None if ring is None else {
+        "ring_attention": ({"skipped": ring_skipped} if ring_skipped else None) if ring is None else {
             "what": "ulysses_ring_attn_fwd + ulysses_ring_attn_bwd on the same inputs: P chunks of all heads, "
                     "P ring steps merged through the log-sum-exp (one GPU: the hops are pointer offsets)",
             "ms_per_step": round(ring["ms_per_step"], 3),
