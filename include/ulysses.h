@@ -47,7 +47,7 @@ extern "C" {
 typedef enum {
     ULY_OK = 0,
     ULY_ERR_INVALID_ARG = 1, /* a size, count or flag is out of range */
-    ULY_ERR_UNSUPPORTED = 2, /* valid for the method, not handled by this build */
+    ULY_ERR_UNSUPPORTED = 2, /* valid for the method, not handled by this library */
     ULY_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
     ULY_ERR_OVERLAP = 4,     /* input and output buffers overlap */
     ULY_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
