@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         // dQ partial: read out of TMEM (frees the dP/dQ columns), then its 8
         // vector reductions (one per group of 4 columns) are spread over the
-        // following work: groups 0-3 while the dP product runs, 4-5 after the
+        // following work: groups 0-2 while the dP product runs, 3-5 after the
         // dS^T hand-off, 6 at the top of the next iteration and 7 in the middle
         // of its P^T computation.  Pushing 64 KB per iteration through the SM's
         // global-reduction path in bursts stalls the warps that are due on the
@@ -532,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 read_dq(it - 1);
-                reduce_groups(0, 4);
+                reduce_groups(0, 3);
             } else {
                 dq_base = nullptr;
             }
@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(ds_full);
-            reduce_groups(4, 6);
+            reduce_groups(3, 6);
         }
         if (ok && n_it > 0) {
             if (mbar_wait_warp(dq_full, (n_it - 1) & 1, p.w, 0x76)) {
