@@ -311,6 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  make_float2(0.f, 0.f)};
                 const bool first = __any_sync(0xffffffffu, m == -INFINITY);
                 if (!first) {
+                    // p = 2^(s * scale * log2(e) - m) on the SFU (masked scores are
+                    // -inf and give exactly 0); the scale-and-shift and the row sum
+                    // run as packed f32x2 pairs, the sum in four independent chains
                     const float2 nm2 = make_float2(-m, -m);
 #pragma unroll
                     for (int c = 0; c < kBN; c += 2) {
