@@ -142,6 +142,69 @@ def whole_job_throughput(world: int, flops_per_rank_step: float, ms_per_step: fl
 
 
 # ------------------------------------------------------------- our arm
+def pipelined_steps(n_steps, stream, up, down, step, sets_in, sets_out, result_of, h_in_of, h_out_of,
+                    one_output_set=False):
+    """Run `n_steps` calls of `step` as a stream of batches, with every step's
+    inputs uploaded from and results read back to pinned host memory.
+
+    Two device input sets alternate: the upload of step i+1 (stream `up`) and
+    the read-back of step i-1 (stream `down`) run while step i computes on
+    `stream`.  A step starts once its Q, K, V are in; dO, first read after the
+    forward, follows them (`before_do`); its O is read back while its backward
+    runs (`after_o`), the rest once the step is done.  `h_in_of(i)` and
+    `h_out_of(i)` give step i's host tensors, `result_of(i)` the device tensors
+    its read-back copies; with `one_output_set` every step writes the same
+    device outputs.  Returns the (start, end) timing events."""
+    import torch
+    ev_in, ev_do, ev_o, ev_done, ev_out = ([torch.cuda.Event() for _ in range(n_steps)] for _ in range(5))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    up.wait_event(e0)
+    down.wait_event(e0)
+
+    def upload(i):
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(ev_done[i - 2])  # step i-2 has consumed this input set
+            hin = h_in_of(i)
+            for dx, hx in zip(sets_in[i % 2][:3], hin[:3]):
+                dx.copy_(hx, non_blocking=True)
+            ev_in[i].record(up)  # Q, K, V
+            sets_in[i % 2][3].copy_(hin[3], non_blocking=True)
+            ev_do[i].record(up)
+
+    def read_back_o(i):
+        ev_o[i].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_o[i])
+            h_out_of(i)[0].copy_(result_of(i)[0], non_blocking=True)
+
+    def read_back(i):
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[i])
+            for hx, dx in zip(h_out_of(i)[1:], result_of(i)[1:]):
+                hx.copy_(dx, non_blocking=True)
+            ev_out[i].record(down)
+
+    upload(0)
+    for i in range(n_steps):
+        if i + 1 < n_steps:
+            upload(i + 1)
+        stream.wait_event(ev_in[i])
+        if i >= 2:
+            stream.wait_event(ev_out[i - 2])  # step i-2's results are out of this output set
+        if one_output_set and i >= 1:
+            stream.wait_event(ev_out[i - 1])
+        step(ins=sets_in[i % 2], outs_seq=sets_out[i % 2], after_o=lambda: read_back_o(i),
+             before_do=lambda: stream.wait_event(ev_do[i]))
+        ev_done[i].record(stream)
+        read_back(i)
+    stream.wait_event(ev_out[n_steps - 1])
+    e1.record(stream)
+    return e0, e1
+
+
 def run_ours(args, rank, world, dist):
     import torch
     import long_context_sequence_head_gb300 as uly
@@ -324,60 +387,13 @@ def run_ours(args, rank, world, dist):
     # a second output set only where the results are written in the seq layout
     sets_out = [outs_main, tuple(torch.empty_like(x) for x in outs_main) if full else outs_main]
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(e_steps)]
-    ev_do = [torch.cuda.Event() for _ in range(e_steps)]
-    ev_o = [torch.cuda.Event() for _ in range(e_steps)]
-    ev_done = [torch.cuda.Event() for _ in range(e_steps)]
-    ev_out = [torch.cuda.Event() for _ in range(e_steps)]
 
     def result_of(i):  # the device tensors step i's read-back copies
         return sets_out[i % 2] if full else outs
 
     barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    up.wait_event(e0)
-    down.wait_event(e0)
-
-    def upload(i):
-        with torch.cuda.stream(up):
-            if i >= 2:
-                up.wait_event(ev_done[i - 2])  # step i-2 has consumed this input set
-            for dx, hx in zip(sets_in[i % 2][:3], h_in[:3]):
-                dx.copy_(hx, non_blocking=True)
-            ev_in[i].record(up)  # Q, K, V
-            sets_in[i % 2][3].copy_(h_in[3], non_blocking=True)
-            ev_do[i].record(up)
-
-    def read_back_o(i):
-        ev_o[i].record(stream)
-        with torch.cuda.stream(down):
-            down.wait_event(ev_o[i])
-            h_out[i % 2][0].copy_(result_of(i)[0], non_blocking=True)
-
-    def read_back(i):
-        with torch.cuda.stream(down):
-            down.wait_event(ev_done[i])
-            for hx, dx in zip(h_out[i % 2][1:], result_of(i)[1:]):
-                hx.copy_(dx, non_blocking=True)
-            ev_out[i].record(down)
-
-    upload(0)
-    for i in range(e_steps):
-        if i + 1 < e_steps:
-            upload(i + 1)
-        stream.wait_event(ev_in[i])
-        if i >= 2:
-            stream.wait_event(ev_out[i - 2])  # step i-2's results are out of this output set
-        if not full and i >= 1:
-            stream.wait_event(ev_out[i - 1])  # one output set only
-        step(ins=sets_in[i % 2], outs_seq=sets_out[i % 2], after_o=lambda: read_back_o(i),
-             before_do=lambda: stream.wait_event(ev_do[i]))
-        ev_done[i].record(stream)
-        read_back(i)
-    stream.wait_event(ev_out[e_steps - 1])
-    e1.record(stream)
+    e0, e1 = pipelined_steps(e_steps, stream, up, down, step, sets_in, sets_out, result_of,
+                             lambda i: h_in, lambda i: h_out[i % 2], one_output_set=not full)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dist, dev)
     # the same work with no overlap: upload, step, read-back on one stream
