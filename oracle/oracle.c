@@ -365,9 +365,13 @@ void oracle_attn_bwd_q_rows(const double *q, const double *k, const double *v, c
     }
 }
 
-/* Sampled dk/dv rows.  keys: nkeys x 4 (s, b, kvh, j).  For every query row
- * i that may attend to key j (in every head of the group) the row's own
- * forward is recomputed, so the cost is (#rows attending j) * N * d. */
+/* Sampled dk/dv rows.  keys: nkeys x 4 (s, b, kvh, j).  First every query
+ * row i of the key's GQA group that may attend to one of the keys gets its
+ * own forward (lse_i, o_i by attn_row) and D_i = <dO_i, o_i>, once even when
+ * several keys share it; then each key sums over its rows with dkv_row, the
+ * same per-key loop the full backward runs.  The result is therefore the
+ * full backward's dk_j, dv_j bit for bit, at a cost of (#distinct attending
+ * rows) * N * d.  dk_rows, dv_rows [nkeys][d]. */
 void oracle_attn_bwd_kv_rows(const double *q, const double *k, const double *v, const double *dout,
                              int64_t S, int64_t B, int64_t N, int64_t Hq, int64_t Hkv, int64_t d,
                              int causal, const int32_t *cu, int ndocs, double scale,
@@ -375,47 +379,50 @@ void oracle_attn_bwd_kv_rows(const double *q, const double *k, const double *v, 
 {
     const shape_t sh = make_shape(S, B, N, Hq, Hkv, d, causal, cu, ndocs, scale);
     const int64_t G = Hq / Hkv;
-    for (int64_t r = 0; r < nkeys * d; r++) {
-        dk_rows[r] = 0.0;
-        dv_rows[r] = 0.0;
-    }
+    const int64_t nq = S * B * Hq * N;
+    /* lse and D indexed [S][B][Hq][N] as in oracle_attn_bwd; only the rows
+     * some key needs are filled */
+    double *lse = (double *)malloc(sizeof(double) * (size_t)nq);
+    double *D = (double *)malloc(sizeof(double) * (size_t)nq);
+    unsigned char *need = (unsigned char *)calloc((size_t)nq, 1);
     for (int64_t r = 0; r < nkeys; r++) {
         const int64_t s = keys[4 * r], b = keys[4 * r + 1], kvh = keys[4 * r + 2], j = keys[4 * r + 3];
-        const double *kj = row_kv(k, &sh, s, b, kvh, j);
-        const double *vj = row_kv(v, &sh, s, b, kvh, j);
-        double *dkj = dk_rows + r * d, *dvj = dv_rows + r * d;
-#pragma omp parallel
-        {
-            double *sbuf = (double *)malloc(sizeof(double) * (size_t)N);
-            double *oi = (double *)malloc(sizeof(double) * (size_t)d);
-            double *dk_loc = (double *)calloc((size_t)d, sizeof(double));
-            double *dv_loc = (double *)calloc((size_t)d, sizeof(double));
-#pragma omp for collapse(2) schedule(dynamic, 1)
-            for (int64_t h = kvh * G; h < (kvh + 1) * G; h++)
-                for (int64_t i = 0; i < N; i++) {
-                    if (!allowed(&sh, i, j))
-                        continue;
-                    const double lse_i = attn_row(q, k, v, &sh, s, b, h, i, oi, sbuf);
-                    const double *qi = row_q(q, &sh, s, b, h, i);
-                    const double *doi = row_q(dout, &sh, s, b, h, i);
-                    const double D_i = dot(doi, oi, d);
-                    const double P = exp(scale * dot(qi, kj, d) - lse_i);
-                    const double dP = dot(doi, vj, d);
-                    const double dS = P * (dP - D_i);
-                    for (int64_t c = 0; c < d; c++) {
-                        dk_loc[c] += scale * dS * qi[c];
-                        dv_loc[c] += P * doi[c];
-                    }
-                }
-#pragma omp critical
-            for (int64_t c = 0; c < d; c++) {
-                dkj[c] += dk_loc[c];
-                dvj[c] += dv_loc[c];
-            }
-            free(dk_loc);
-            free(dv_loc);
-            free(oi);
-            free(sbuf);
-        }
+        for (int64_t h = kvh * G; h < (kvh + 1) * G; h++)
+            for (int64_t i = 0; i < N; i++)
+                if (allowed(&sh, i, j))
+                    need[((s * B + b) * Hq + h) * N + i] = 1;
     }
+    int64_t nneed = 0;
+    for (int64_t idx = 0; idx < nq; idx++)
+        nneed += need[idx];
+    int64_t *list = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nneed > 0 ? nneed : 1));
+    nneed = 0;
+    for (int64_t idx = 0; idx < nq; idx++)
+        if (need[idx])
+            list[nneed++] = idx;
+#pragma omp parallel
+    {
+        double *sbuf = (double *)malloc(sizeof(double) * (size_t)N);
+        double *oi = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t t = 0; t < nneed; t++) {
+            const int64_t idx = list[t];
+            const int64_t i = idx % N;
+            const int64_t h = (idx / N) % Hq;
+            const int64_t b = (idx / (N * Hq)) % B;
+            const int64_t s = idx / (N * Hq * B);
+            lse[idx] = attn_row(q, k, v, &sh, s, b, h, i, oi, sbuf);
+            D[idx] = dot(row_q(dout, &sh, s, b, h, i), oi, d);
+        }
+        free(oi);
+        free(sbuf);
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nkeys; r++)
+        dkv_row(q, k, v, dout, lse, D, &sh, keys[4 * r], keys[4 * r + 1], keys[4 * r + 2], keys[4 * r + 3],
+                dk_rows + r * d, dv_rows + r * d);
+    free(list);
+    free(need);
+    free(D);
+    free(lse);
 }

@@ -117,11 +117,30 @@ def test_rows_equal_full(oracle_mod):
     dq_r = oracle_mod.attn_bwd_q_rows(q, k, v, do, rows, cu_seqlens=cu)
     for n, (s, b, h, i) in enumerate(rows):
         np.testing.assert_allclose(dq_r[n], dq[s, b, i, h], rtol=1e-13, atol=1e-14)
-    keys = [(1, 1, 1, 14), (0, 0, 0, 0), (0, 1, 1, 8), (1, 0, 0, 3)]
+    # keys sharing their attending rows (same shard, batch and KV head) and
+    # one repeated key: each row's forward is computed once and every key sums
+    # over its rows as the full backward does, so the rows are bit-identical
+    keys = [(1, 1, 1, 14), (0, 0, 0, 0), (0, 1, 1, 8), (1, 0, 0, 3), (1, 0, 0, 5), (1, 0, 0, 3)]
     dk_r, dv_r = oracle_mod.attn_bwd_kv_rows(q, k, v, do, keys, cu_seqlens=cu)
     for n, (s, b, kvh, j) in enumerate(keys):
-        np.testing.assert_allclose(dk_r[n], dk[s, b, j, kvh], rtol=1e-12, atol=1e-13)
-        np.testing.assert_allclose(dv_r[n], dv[s, b, j, kvh], rtol=1e-12, atol=1e-13)
+        assert np.array_equal(dk_r[n], dk[s, b, j, kvh]), (n, dk_r[n], dk[s, b, j, kvh])
+        assert np.array_equal(dv_r[n], dv[s, b, j, kvh]), (n, dv_r[n], dv[s, b, j, kvh])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_kv_rows_of_one_group_equal_full(oracle_mod, causal):
+    """Every key of one (shard, batch, KV head), so all attending rows are
+    shared between keys: still the full backward's rows bit for bit."""
+    S, B, N, Hq, Hkv, d = 1, 1, 21, 6, 2, 4
+    q = _randn((S, B, N, Hq, d), 21)
+    k = _randn((S, B, N, Hkv, d), 22)
+    v = _randn((S, B, N, Hkv, d), 23)
+    do = _randn((S, B, N, Hq, d), 24)
+    dq, dk, dv, _, _ = oracle_mod.attn_bwd(q, k, v, do, causal=causal)
+    keys = [(0, 0, 1, j) for j in range(N)]
+    dk_r, dv_r = oracle_mod.attn_bwd_kv_rows(q, k, v, do, keys, causal=causal)
+    assert np.array_equal(dk_r, dk[0, 0, :, 1])
+    assert np.array_equal(dv_r, dv[0, 0, :, 1])
 
 
 def test_ulysses_sharded_grads_equal_unsharded(oracle_mod):
