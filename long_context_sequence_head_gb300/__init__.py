@@ -31,7 +31,7 @@ _STATUS = {0: "ULY_OK", 1: "ULY_ERR_INVALID_ARG", 2: "ULY_ERR_UNSUPPORTED", 3: "
            8: "ULY_ERR_SCRATCH_LIMIT"}
 
 # every symbol include/ulysses.h declares
-EXPORTED = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_workspace_size",
+EXPORTED = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_swap_batch", "ulysses_attn_workspace_size",
             "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_attn_fwd_seq", "ulysses_attn_bwd_seq",
             "ulysses_attn_bwd_noalloc", "ulysses_sharded_ce_workspace_size", "ulysses_sharded_ce_loss",
             "ulysses_ring_attn_workspace_size", "ulysses_ring_attn_fwd", "ulysses_ring_attn_bwd",
@@ -69,6 +69,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     sz = ctypes.c_size_t
     lib.ulysses_seq_to_head.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, vp]
     lib.ulysses_head_to_seq.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, vp]
+    lib.ulysses_swap_batch.argtypes = [vp, i32, i64, i64, i32, i32, i32, vp]
     lib.ulysses_attn_workspace_size.argtypes = [i64, i64, i32, i32, i32, i32, i32, i32, i32]
     lib.ulysses_attn_workspace_size.restype = sz
     lib.ulysses_attn_fwd.argtypes = [vp] * 5 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp, sz, vp]
@@ -92,7 +93,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.ulysses_status_string.argtypes = [i32]
     lib.ulysses_status_string.restype = ctypes.c_char_p
     lib.ulysses_version.restype = i32
-    for name in ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_attn_fwd", "ulysses_attn_bwd",
+    for name in ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_swap_batch", "ulysses_attn_fwd",
+                 "ulysses_attn_bwd",
                  "ulysses_attn_bwd_noalloc", "ulysses_attn_fwd_seq", "ulysses_attn_bwd_seq",
                  "ulysses_get_device_status", "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout"):
         getattr(lib, name).restype = i32
@@ -188,6 +190,46 @@ def ulysses_head_to_seq(x_head: torch.Tensor, x_seq: torch.Tensor, P: int, strea
     _check("ulysses_head_to_seq", load().ulysses_head_to_seq(
         x_head.data_ptr(), x_seq.data_ptr(), B, N, Hp * P, d, P, _dt(x_head), _stream(stream)))
     return x_seq
+
+
+class _SwapDesc(ctypes.Structure):
+    _fields_ = [("src", ctypes.c_void_p), ("dst", ctypes.c_void_p), ("H", ctypes.c_int32),
+                ("to_head", ctypes.c_int32)]
+
+
+def ulysses_swap_batch(items, P: int, stream=None):
+    """Up to four swaps in one launch (see include/ulysses.h).  items: a
+    sequence of (src, dst, to_head); to_head=True takes a seq-layout src
+    [P][B][N/P][H][d] to a head-layout dst [P][B][N][H/P][d], False the
+    reverse.  All tensors share B, N, d, P and dtype."""
+    items = list(items)
+    if not 1 <= len(items) <= 4:
+        raise ValueError("a swap batch holds 1 to 4 tensors")
+    descs = (_SwapDesc * len(items))()
+    shape = None
+    dtype = None
+    for i, (src, dst, to_head) in enumerate(items):
+        _dev(src, dst)
+        if to_head:
+            Ps, B, Np, H, d = src.shape
+            want = (P, B, Np * P, H // P, d)
+            got = tuple(dst.shape)
+        else:
+            Ps, B, N_, Hp, d = src.shape
+            Np, H = N_ // P, Hp * P
+            want = (P, B, Np, H, d)
+            got = tuple(dst.shape)
+        if Ps != P or got != want or dst.dtype != src.dtype:
+            raise ValueError(f"item {i}: expected a destination of shape {want} and the source dtype, got {got}")
+        if shape is None:
+            shape, dtype = (B, Np * P, d), src.dtype
+        elif (B, Np * P, d) != shape or src.dtype != dtype:
+            raise ValueError("all tensors of a batch share B, N, d and dtype")
+        descs[i] = _SwapDesc(src.data_ptr(), dst.data_ptr(), H, 1 if to_head else 0)
+    B, N, d = shape
+    _check("ulysses_swap_batch", load().ulysses_swap_batch(
+        ctypes.cast(descs, ctypes.c_void_p), len(items), B, N, d, P, ULY_BF16 if dtype == torch.bfloat16
+        else ULY_FP32, _stream(stream)))
 
 
 # -------------------------------------------------------------- attention
@@ -290,17 +332,25 @@ def ulysses_attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = T
                              stream=None):
     """Attention backward without a workspace, for callers that cannot
     allocate device memory; its scratch is a fixed 64 MiB array inside the
-    library (see include/ulysses.h for the limits and the ordering rule)."""
+    library (see include/ulysses.h for the limits and the ordering rule).
+    The call runs with q's device current, since the library takes the
+    scratch address of the current device."""
     _attn_args(q, k, v, like_q=(o, dout, dq), like_k=(dk, dv), lse=lse,
                lse_shape=(q.shape[0], q.shape[1], q.shape[3], q.shape[2]))
     _dev(q, k, v, o, lse, dout, dq, dk, dv)
+    for t in (k, v, o, lse, dout, dq, dk, dv):
+        if t.device != q.device:
+            raise ValueError("all tensors must live on q's device")
+    if isinstance(stream, torch.cuda.Stream) and stream.device != q.device:
+        raise ValueError("the stream must belong to q's device")
     S, B, N, Hq, d = q.shape
     Hkv = k.shape[3]
     cu_p, nd, _keep = _cu(cu_seqlens)
-    _check("ulysses_attn_bwd_noalloc", load().ulysses_attn_bwd_noalloc(
-        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
-        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, N, Hq, Hkv, d, S, int(bool(causal)), cu_p, nd,
-        float(softmax_scale), _dt(q), _stream(stream)))
+    with torch.cuda.device(q.device):
+        _check("ulysses_attn_bwd_noalloc", load().ulysses_attn_bwd_noalloc(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, N, Hq, Hkv, d, S, int(bool(causal)), cu_p, nd,
+            float(softmax_scale), _dt(q), _stream(stream)))
     return dq, dk, dv
 
 
@@ -347,12 +397,14 @@ def ulysses_ring_attn_bwd(q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_
 # ---------------------------------------------------------- sharded loss
 
 def ulysses_sharded_ce_loss(logits, labels, P: int, dlogits: Optional[torch.Tensor] = None,
-                            workspace: Optional[torch.Tensor] = None, stream=None):
+                            workspace: Optional[torch.Tensor] = None, stream=None,
+                            outputs: Optional[Sequence[torch.Tensor]] = None):
     """Shifted next-token CE per rank and its good-token-weighted aggregation.
 
     logits [P][B][N/P][V] (bf16/fp32), labels [P][B][N/P] int64 (unshifted,
     -100 = ignored).  Returns (shard_loss [P] fp32, shard_good [P] int64,
     total [1] fp32) on the device; fills dlogits (like logits) if given.
+    `outputs` may supply those three tensors (else they are allocated).
     """
     if logits.dim() != 4 or logits.shape[0] != P:
         raise ValueError(f"logits must be [P={P}][B][N/P][V], got {tuple(logits.shape)}")
@@ -366,9 +418,16 @@ def ulysses_sharded_ce_loss(logits, labels, P: int, dlogits: Optional[torch.Tens
     if labels.dtype != torch.int64 or tuple(labels.shape) != (P, B, Np):
         raise ValueError("labels must be int64 [P][B][N/P]")
     dev = logits.device
-    shard_loss = torch.empty(P, dtype=torch.float32, device=dev)
-    shard_good = torch.empty(P, dtype=torch.int64, device=dev)
-    total = torch.empty(4, dtype=torch.float32, device=dev)
+    if outputs is None:
+        shard_loss = torch.empty(P, dtype=torch.float32, device=dev)
+        shard_good = torch.empty(P, dtype=torch.int64, device=dev)
+        total = torch.empty(4, dtype=torch.float32, device=dev)
+    else:
+        shard_loss, shard_good, total = outputs
+        if (shard_loss.dtype != torch.float32 or shard_loss.numel() != P or shard_good.dtype != torch.int64
+                or shard_good.numel() != P or total.dtype != torch.float32 or total.numel() < 1):
+            raise ValueError("outputs must be (fp32 [P], int64 [P], fp32 [>=1])")
+        _dev(shard_loss, shard_good, total)
     need = int(load().ulysses_sharded_ce_workspace_size(B, N, P))
     ws = _workspace(workspace, need, dev)
     _check("ulysses_sharded_ce_loss", load().ulysses_sharded_ce_loss(

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from parity_utils import LSE_TOL, REL_TOL, bytes_equal, log_errors, max_abs, rel_fro, run_path
+from parity_utils import LSE_TOL, REL_TOL, Guards, bytes_equal, log_errors, max_abs, rel_fro, run_path
 from ulysses_inputs import WORKLOADS, draw_seq_inputs
 
 pytestmark = pytest.mark.gpu
@@ -36,13 +36,19 @@ def _attn_inputs_case(uly, q, k, v, do, causal, cu, label="", tol=None):
     Hkv = k.shape[3]
     tag = "bf16" if q.dtype == torch.bfloat16 else "fp32"
     qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
-    o = torch.full_like(qd, float("nan"))
-    lse = torch.full((S, B, Hq, N), float("nan"), dtype=torch.float32, device="cuda")
-    uly.ulysses_attn_fwd(qd, kd, vd, o, lse, causal=causal, cu_seqlens=cu)
-    dq, dk, dv = (torch.full_like(x, float("nan")) for x in (qd, kd, vd))
-    uly.ulysses_attn_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, causal=causal, cu_seqlens=cu)
+    g = Guards()
+    nd = 0 if cu is None else len(cu) - 1
+    o = g.full_like(qd, float("nan"))
+    lse = g.empty((S, B, Hq, N), torch.float32, float("nan"))
+    ws_f = g.workspace(uly.ulysses_attn_workspace_size(B, N, Hq, Hkv, d, S, nd, False, q.dtype))
+    uly.ulysses_attn_fwd(qd, kd, vd, o, lse, causal=causal, cu_seqlens=cu, workspace=ws_f)
+    g.check()
+    dq, dk, dv = (g.full_like(x, float("nan")) for x in (qd, kd, vd))
+    ws_b = g.workspace(uly.ulysses_attn_workspace_size(B, N, Hq, Hkv, d, S, nd, True, q.dtype))
+    uly.ulysses_attn_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, causal=causal, cu_seqlens=cu, workspace=ws_b)
     torch.cuda.synchronize()
     assert uly.ulysses_get_device_status()[0] == 0
+    g.check()
     dq_r, dk_r, dv_r, o_r, lse_r = oracle.attn_bwd(q, k, v, do, causal=causal, cu_seqlens=cu)
     # with one token dS = dP - D vanishes: dQ and dK are exactly 0, so their
     # error is measured against the size of the other gradients instead
@@ -252,10 +258,12 @@ def test_one_token_documents_copy_values(uly):
     q = _rand((1, 1, N, Hq, 128), 7, torch.bfloat16).cuda()
     k = _rand((1, 1, N, Hkv, 128), 8, torch.bfloat16).cuda()
     v = _rand((1, 1, N, Hkv, 128), 9, torch.bfloat16).cuda()
-    o = torch.empty_like(q)
-    lse = torch.empty(1, 1, Hq, N, dtype=torch.float32, device="cuda")
+    g = Guards()
+    o = g.empty(q.shape, q.dtype)
+    lse = g.empty((1, 1, Hq, N), torch.float32)
     uly.ulysses_attn_fwd(q, k, v, o, lse, causal=True, cu_seqlens=cu)
     torch.cuda.synchronize()
+    g.check()
     for h in range(Hq):
         assert torch.equal(o[0, 0, :, h], v[0, 0, :, 0])
 

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from parity_utils import LSE_TOL, REL_TOL, bytes_equal, log_errors, max_abs, rel_fro
+from parity_utils import LSE_TOL, REL_TOL, Guards, bytes_equal, log_errors, max_abs, rel_fro
 from ulysses_inputs import WORKLOADS, cu_seqlens_from_lengths, draw_seq_inputs
 
 pytestmark = pytest.mark.gpu
@@ -15,13 +15,15 @@ def _run_fused(uly, seq, P, cu=None):
     q, k, v, do = (seq[n].cuda() for n in ("q", "k", "v", "dout"))
     Ps, B, Np, Hq, d = q.shape
     N = Np * P
-    o = torch.full_like(q, float("nan"))
-    lse = torch.full((P, B, Hq // P, N), float("nan"), dtype=torch.float32, device="cuda")
+    g = Guards()
+    o = g.full_like(q, float("nan"))
+    lse = g.empty((P, B, Hq // P, N), torch.float32, float("nan"))
     uly.ulysses_attn_fwd_seq(q, k, v, o, lse, P, cu_seqlens=cu)
-    dq, dk, dv = (torch.full_like(x, float("nan")) for x in (q, k, v))
+    dq, dk, dv = (g.full_like(x, float("nan")) for x in (q, k, v))
     uly.ulysses_attn_bwd_seq(q, k, v, o, lse, do, dq, dk, dv, P, cu_seqlens=cu)
     torch.cuda.synchronize()
     assert uly.ulysses_get_device_status()[0] == 0
+    g.check()
     return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
 
 

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from parity_utils import LSE_TOL, REL_TOL, log_errors, max_abs, rel_fro
+from parity_utils import LSE_TOL, REL_TOL, Guards, log_errors, max_abs, rel_fro
 from ulysses_inputs import WORKLOADS, draw_seq_inputs
 
 pytestmark = pytest.mark.gpu
@@ -15,13 +15,19 @@ pytestmark = pytest.mark.gpu
 def _ring(uly, seq, P, causal=True):
     q, k, v, do = (seq[n].cuda() for n in ("q", "k", "v", "dout"))
     Ps, B, Np, Hq, d = q.shape
-    o = torch.full_like(q, float("nan"))
-    lse = torch.full((P, B, Hq, Np), float("nan"), dtype=torch.float32, device="cuda")
-    uly.ulysses_ring_attn_fwd(q, k, v, o, lse, P, causal=causal)
-    dq, dk, dv = (torch.full_like(x, float("nan")) for x in (q, k, v))
-    uly.ulysses_ring_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, P, causal=causal)
+    Hkv = k.shape[3]
+    g = Guards()
+    o = g.full_like(q, float("nan"))
+    lse = g.empty((P, B, Hq, Np), torch.float32, float("nan"))
+    dt = 0 if q.dtype == torch.bfloat16 else 1
+    ws_f = g.workspace(uly.load().ulysses_ring_attn_workspace_size(B, Np * P, Hq, Hkv, d, P, 0, dt))
+    uly.ulysses_ring_attn_fwd(q, k, v, o, lse, P, causal=causal, workspace=ws_f)
+    dq, dk, dv = (g.full_like(x, float("nan")) for x in (q, k, v))
+    ws_b = g.workspace(uly.load().ulysses_ring_attn_workspace_size(B, Np * P, Hq, Hkv, d, P, 1, dt))
+    uly.ulysses_ring_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, P, causal=causal, workspace=ws_b)
     torch.cuda.synchronize()
     assert uly.ulysses_get_device_status()[0] == 0
+    g.check()
     return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
 
 

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from parity_utils import REL_TOL, log_errors, rel_fro
+from parity_utils import REL_TOL, Guards, log_errors, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -47,10 +47,15 @@ def _oracle(logits, labels, P):
 ])
 def test_sharded_ce_vs_oracle(uly, P, B, N, V, dtype):
     logits, labels = _case(P, B, N, V, dtype, seed=N + V)
-    dl = torch.full(logits.shape, float("nan"), dtype=dtype, device="cuda")
-    sl, sg, tot = uly.ulysses_sharded_ce_loss(logits.cuda(), labels.cuda(), P, dlogits=dl)
+    g = Guards()
+    dl = g.empty(logits.shape, dtype, float("nan"))
+    outs = (g.empty((P,), torch.float32), g.empty((P,), torch.int64), g.empty((1,), torch.float32))
+    ws = g.workspace(uly.load().ulysses_sharded_ce_workspace_size(B, N, P))
+    sl, sg, tot = uly.ulysses_sharded_ce_loss(logits.cuda(), labels.cuda(), P, dlogits=dl, workspace=ws,
+                                              outputs=outs)
     torch.cuda.synchronize()
     assert uly.ulysses_get_device_status()[0] == 0
+    g.check()
     losses, goods, total, grad = _oracle(logits, labels, P)
     assert sg.cpu().numpy().tolist() == goods.tolist()
     tag = "bf16" if dtype == torch.bfloat16 else "fp32"
