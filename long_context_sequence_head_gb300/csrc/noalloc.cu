@@ -11,12 +11,16 @@
 // Here that scratch is one file-scope device array of a fixed size.  Any GPU
 // that loads this part of the library holds it until the process exits.  Its
 // device address is looked up once per device with cudaGetSymbolAddress (the
-// array's name in host code is only a host-side stand-in); the lookup happens
-// on the first call on each device, which therefore must come before any
-// stream capture.  Every call shares the array and it keeps the previous
-// call's contents; the backward rewrites or clears every byte it reads before
-// reading it.  Calls that overlap on the GPU (different streams, or threads
-// without ordering) race on the array and must not be issued.
+// array's name in host code is only a host-side stand-in).  The runtime loads
+// device code lazily, so that lookup, on the first call on each device, is
+// what loads this module and makes the driver reserve the array: a caller
+// that cannot afford the reservation inside its restricted context makes its
+// first call on each device outside it, and before any stream capture.  The
+// address is the current device's, so the stream and every pointer must
+// belong to the current device.  Every call shares the array and it keeps the
+// previous call's contents; the backward rewrites or clears every byte it
+// reads before reading it.  Calls that overlap on the GPU (different streams,
+// or threads without ordering) race on the array and must not be issued.
 #include <ulysses.h>
 
 #include <mutex>
