@@ -90,6 +90,32 @@ uly_status ulysses_seq_to_head(const void *x_seq, void *x_head, int64_t B, int64
 uly_status ulysses_head_to_seq(const void *x_head, void *x_seq, int64_t B, int64_t N, int32_t H,
                                int32_t d, int32_t P, uly_dtype dtype, void *stream);
 
+/*
+ * A batch of up to four swaps in one launch, e.g. Q, K and V on their way to
+ * the head layout (the all-to-all diagram moves them together), dQ, dK and dV
+ * on their way back, or O going back while dO comes in.  Every tensor of the
+ * batch shares B, N, d, P and dtype; each has its own head count H and its
+ * own direction.  The results are those of the single calls, bit for bit.
+ *
+ * descs_host : host array of n_descs entries (1 <= n_descs <= 4), read before
+ *              the call returns:
+ *   src, dst : device buffers as in ulysses_seq_to_head (to_head = 1) or
+ *              ulysses_head_to_seq (to_head = 0);
+ *   H        : the tensor's head count, H % P == 0.
+ * Same argument rules as ulysses_seq_to_head for every entry.  In addition no
+ * entry's dst may overlap another entry's src or dst (ULY_ERR_OVERLAP): the
+ * entries are copied concurrently.
+ */
+typedef struct {
+    const void *src;
+    void *dst;
+    int32_t H;
+    int32_t to_head;
+} uly_swap_desc;
+
+uly_status ulysses_swap_batch(const uly_swap_desc *descs_host, int32_t n_descs, int64_t B, int64_t N,
+                              int32_t d, int32_t P, uly_dtype dtype, void *stream);
+
 /* ------------------------------------------------------------ attention */
 
 /*
@@ -204,12 +230,21 @@ uly_status ulysses_attn_bwd_seq(const void *q_seq, const void *k_seq, const void
  * exceeds 64 MiB return ULY_ERR_SCRATCH_LIMIT and launch nothing; for bf16
  * that is about 129,000 (shard x batch x query-head x padded-row) rows, e.g.
  * N = 8192 with 8 local query heads and 1 shard fits.
- * The call allocates nothing (no cudaMalloc, no allocating library routine).
- * The first call on a device looks up the array's device address; make that
- * first call before any stream capture.  All calls share the array: calls
- * that overlap on the GPU (other streams, other threads) race and must not
- * be issued; sequential calls are safe because each one rewrites or clears
- * every scratch byte it reads.
+ * The call itself makes no cudaMalloc and calls no allocating library
+ * routine.  The array is part of the library's device code, which the CUDA
+ * runtime loads onto a device lazily: the first call on each device looks up
+ * the array's device address, and that lookup loads the module, so the
+ * driver reserves the 64 MiB (and the module's code) inside that first call.
+ * A caller whose restricted context cannot afford that reservation (a fixed
+ * pool with its memory already committed, an allocator hook) must make the
+ * first call on each device outside that context, at start-up, and also
+ * before any stream capture; later calls reserve nothing.
+ * stream and every pointer must belong to the CURRENT device (the scratch
+ * address is the current device's).  After cudaDeviceReset the cached
+ * address is stale: do not call this entry point again in that process.
+ * All calls share the array: calls that overlap on the GPU (other streams,
+ * other threads) race and must not be issued; sequential calls are safe
+ * because each one rewrites or clears every scratch byte it reads.
  */
 uly_status ulysses_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                                     const float *lse, const void *dout, void *dq, void *dk, void *dv,

@@ -18,6 +18,14 @@
 // independent rings of 32 KB stages keep more transfers in flight than one
 // thread alone issues); rows too large for three stages in half the shared
 // memory run one CTA per SM instead.
+//
+// One launch moves a batch of up to four tensors that share B, N, d, P and
+// the dtype (Q, K and V have different head counts; O going back while dO
+// comes in are two directions): their work items form one list that every
+// CTA strides through, so small tensors do not each pay a launch's fill and
+// drain (the all-to-all diagram exchanges Q, K and V together).
+#include <cstring>
+
 #include "uly_internal.h"
 
 namespace uly {
@@ -37,22 +45,33 @@ __device__ __forceinline__ void tma_store_5d(const CUtensorMap *map, const void 
         : "memory");
 }
 
-struct SwapParams {
+// One tensor of a batch.
+struct SwapTensor {
     uint8_t *head;       // head-layout buffer (src for head->seq, dst for seq->head)
+    int64_t row_bytes;   // Hp * d * esize: one token of one head block
+    int64_t nchunks;     // ceil(Np / T)
+    int64_t item0;       // first item of this tensor in the batch's list
+    int64_t nitems;      // P (src shard) * B * nchunks * P (dst head block)
+    int T;               // tokens per work item (TMA box height)
+    int to_head;         // 1: seq->head, 0: head->seq
+};
+
+struct SwapParams {
+    CUtensorMap maps[kSwapMaxBatch];  // 5-D maps over each tensor's seq buffer
+    SwapTensor t[kSwapMaxBatch];
+    int ntensors;
     int64_t B, N, Np;    // batch, tokens, tokens per shard
     int P;               // virtual ranks
-    int64_t row_bytes;   // Hp * d * esize: one token of one head block
-    int T;               // tokens per work item (TMA box height)
-    int64_t nchunks;     // ceil(Np / T)
-    int64_t nitems;      // P (src shard) * B * nchunks * P (dst head block)
+    int64_t nitems;      // all tensors
     int stages;
-    uint32_t stage_bytes;  // T * row_bytes
+    uint32_t stage_alloc;  // bytes between stages
     WaitCfg w;
 };
 
-// item -> (s, b, chunk, r); consecutive items share the seq-side chunk.
+// global item -> (tensor, s, b, chunk, r); consecutive items of a tensor
+// share the seq-side chunk.
 struct Item {
-    int s, b, r;
+    int tn, s, b, r;
     int64_t t0;
     int nt;
 };
@@ -60,27 +79,33 @@ struct Item {
 __device__ __forceinline__ Item decode(const SwapParams &p, int64_t it)
 {
     Item x;
-    x.r = static_cast<int>(it % p.P);
-    int64_t rest = it / p.P;
-    const int64_t c = rest % p.nchunks;
-    rest /= p.nchunks;
+    x.tn = 0;
+#pragma unroll 1
+    while (x.tn + 1 < p.ntensors && it >= p.t[x.tn + 1].item0)
+        ++x.tn;
+    const SwapTensor &t = p.t[x.tn];
+    int64_t rest = it - t.item0;
+    x.r = static_cast<int>(rest % p.P);
+    rest /= p.P;
+    const int64_t c = rest % t.nchunks;
+    rest /= t.nchunks;
     x.b = static_cast<int>(rest % p.B);
     x.s = static_cast<int>(rest / p.B);
-    x.t0 = c * p.T;
+    x.t0 = c * t.T;
     const int64_t left = p.Np - x.t0;
-    x.nt = static_cast<int>(left < p.T ? left : p.T);
+    x.nt = static_cast<int>(left < t.T ? left : t.T);
     return x;
 }
 
 __device__ __forceinline__ uint8_t *head_ptr(const SwapParams &p, const Item &x)
 {
     // head[r][b][s*Np + t0] : contiguous nt * row_bytes
-    return p.head + ((static_cast<int64_t>(x.r) * p.B + x.b) * p.N + static_cast<int64_t>(x.s) * p.Np + x.t0) *
-                        p.row_bytes;
+    const SwapTensor &t = p.t[x.tn];
+    return t.head + ((static_cast<int64_t>(x.r) * p.B + x.b) * p.N + static_cast<int64_t>(x.s) * p.Np + x.t0) *
+                        t.row_bytes;
 }
 
-template <bool kToHead>
-__global__ void __launch_bounds__(32, 1) swap_kernel(const __grid_constant__ CUtensorMap seq_map, SwapParams p)
+__global__ void __launch_bounds__(32, 1) swap_kernel(const __grid_constant__ SwapParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full[kSwapMaxStages];
@@ -96,18 +121,21 @@ __global__ void __launch_bounds__(32, 1) swap_kernel(const __grid_constant__ CUt
     for (int i = 0; i < p.stages; ++i)
         mbar_init(&full[i], 1);
     fence_mbar_init();
-    prefetch_tmap(&seq_map);
+    for (int i = 0; i < p.ntensors; ++i)
+        prefetch_tmap(&p.maps[i]);
 
     auto issue_load = [&](int64_t k) {
         const int st = static_cast<int>(k % p.stages);
         const Item x = decode(p, first + k * stride);
-        uint8_t *buf = smem + static_cast<int64_t>(st) * p.stage_bytes;
-        if (kToHead) {
+        const SwapTensor &t = p.t[x.tn];
+        uint8_t *buf = smem + static_cast<int64_t>(st) * p.stage_alloc;
+        if (t.to_head) {
             // strided seq-side gather: box {d, Hp, 1, T, 1}; rows past Np are zero-filled
-            mbar_expect_tx(&full[st], p.stage_bytes);
-            tma_load_5d(buf, &seq_map, &full[st], 0, 0, x.r, static_cast<int>(x.t0), x.s * static_cast<int>(p.B) + x.b);
+            mbar_expect_tx(&full[st], static_cast<uint32_t>(t.T * t.row_bytes));
+            tma_load_5d(buf, &p.maps[x.tn], &full[st], 0, 0, x.r, static_cast<int>(x.t0),
+                        x.s * static_cast<int>(p.B) + x.b);
         } else {
-            const uint32_t bytes = static_cast<uint32_t>(x.nt * p.row_bytes);
+            const uint32_t bytes = static_cast<uint32_t>(x.nt * t.row_bytes);
             mbar_expect_tx(&full[st], bytes);
             bulk_g2s(buf, head_ptr(p, x), bytes, &full[st]);
         }
@@ -121,18 +149,19 @@ __global__ void __launch_bounds__(32, 1) swap_kernel(const __grid_constant__ CUt
     bool ok = true;
     for (; k < n_local; ++k) {
         const int st = static_cast<int>(k % p.stages);
-        if (!mbar_wait(&full[st], static_cast<uint32_t>((k / p.stages) & 1), p.w, kToHead ? 0x11 : 0x12)) {
+        const Item x = decode(p, first + k * stride);
+        const SwapTensor &t = p.t[x.tn];
+        if (!mbar_wait(&full[st], static_cast<uint32_t>((k / p.stages) & 1), p.w, t.to_head ? 0x11 : 0x12)) {
             ok = false;
             break;
         }
-        const Item x = decode(p, first + k * stride);
-        const uint8_t *buf = smem + static_cast<int64_t>(st) * p.stage_bytes;
-        if (kToHead) {
-            bulk_s2g(head_ptr(p, x), buf, static_cast<uint32_t>(x.nt * p.row_bytes));
+        const uint8_t *buf = smem + static_cast<int64_t>(st) * p.stage_alloc;
+        if (t.to_head) {
+            bulk_s2g(head_ptr(p, x), buf, static_cast<uint32_t>(x.nt * t.row_bytes));
         } else {
             // strided seq-side scatter; tokens past Np are clipped by the map
             fence_async_smem();
-            tma_store_5d(&seq_map, buf, 0, 0, x.r, static_cast<int>(x.t0), x.s * static_cast<int>(p.B) + x.b);
+            tma_store_5d(&p.maps[x.tn], buf, 0, 0, x.r, static_cast<int>(x.t0), x.s * static_cast<int>(p.B) + x.b);
         }
         bulk_commit();
         // refill the stage released by the previous item's store; with a
@@ -154,16 +183,9 @@ __global__ void __launch_bounds__(32, 1) swap_kernel(const __grid_constant__ CUt
     bulk_wait_all<0>();
 }
 
-}  // namespace
-
-cudaError_t launch_swap(bool to_head, const void *src, void *dst, int64_t B, int64_t N, int H, int d, int P,
-                        int esize, cudaStream_t stream)
+// Tokens per work item for rows of row_bytes: about 32 KB per item.
+int tokens_per_item(int64_t row_bytes, int64_t Np)
 {
-    const int Hp = H / P;
-    const int64_t Np = N / P;
-    const int64_t row_bytes = static_cast<int64_t>(Hp) * d * esize;
-    if (row_bytes > kSwapSmemBytes || Hp > 256 || d > 256)
-        return cudaErrorInvalidValue;
     int T = static_cast<int>(32768 / row_bytes);
     if (T < 1)
         T = 1;
@@ -171,62 +193,91 @@ cudaError_t launch_swap(bool to_head, const void *src, void *dst, int64_t B, int
         T = 256;
     if (T > Np)
         T = static_cast<int>(Np);
-    const uint32_t stage_bytes = static_cast<uint32_t>(T * row_bytes);
-    const uint32_t stage_alloc = (stage_bytes + 1023) & ~1023u;
+    return T;
+}
+
+}  // namespace
+
+cudaError_t launch_swap_batch(const SwapDesc *descs, int n, int64_t B, int64_t N, int d, int P, int esize,
+                              cudaStream_t stream)
+{
+    if (n < 1 || n > kSwapMaxBatch)
+        return cudaErrorInvalidValue;
+    const int64_t Np = N / P;
+    SwapParams p;
+    memset(&p, 0, sizeof(p));
+    p.ntensors = n;
+    p.B = B;
+    p.N = N;
+    p.Np = Np;
+    p.P = P;
+    p.w = wait_cfg();
+    uint32_t stage_alloc = 0;
+    int64_t items = 0;
+    for (int i = 0; i < n; ++i) {
+        const int H = descs[i].H;
+        const int Hp = H / P;
+        const int64_t row_bytes = static_cast<int64_t>(Hp) * d * esize;
+        if (row_bytes > kSwapSmemBytes || Hp > 256 || d > 256)
+            return cudaErrorInvalidValue;
+        const int T = tokens_per_item(row_bytes, Np);
+        const uint32_t stage_bytes = static_cast<uint32_t>(T * row_bytes);
+        const uint32_t a = (stage_bytes + 1023) & ~1023u;
+        stage_alloc = a > stage_alloc ? a : stage_alloc;
+
+        // 5-D map over the seq buffer: {d, Hp, P, Np, P*B}, box {d, Hp, 1, T, 1}
+        const bool to_head = descs[i].to_head != 0;
+        const uint8_t *seq = static_cast<const uint8_t *>(to_head ? descs[i].src : descs[i].dst);
+        const CUtensorMapDataType dt = esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32;
+        cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hp), static_cast<cuuint64_t>(P),
+                              static_cast<cuuint64_t>(Np), static_cast<cuuint64_t>(P) * static_cast<cuuint64_t>(B)};
+        cuuint64_t strides[4] = {static_cast<cuuint64_t>(d) * esize, static_cast<cuuint64_t>(row_bytes),
+                                 static_cast<cuuint64_t>(H) * d * esize,
+                                 static_cast<cuuint64_t>(Np) * H * d * esize};
+        cuuint32_t box[5] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(Hp), 1, static_cast<cuuint32_t>(T),
+                             1};
+        cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        CUresult cr = tensor_map_encoder()(&p.maps[i], dt, 5, const_cast<uint8_t *>(seq), dims, strides, box, estr,
+                                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+
+        SwapTensor &t = p.t[i];
+        t.head = static_cast<uint8_t *>(to_head ? descs[i].dst : const_cast<void *>(descs[i].src));
+        t.row_bytes = row_bytes;
+        t.T = T;
+        t.nchunks = (Np + T - 1) / T;
+        t.item0 = items;
+        t.nitems = static_cast<int64_t>(P) * B * t.nchunks * P;
+        t.to_head = to_head ? 1 : 0;
+        items += t.nitems;
+    }
+    p.nitems = items;
     // two CTAs per SM with half the ring each, unless that leaves fewer than three stages
     const bool pair = kSwapPairRing / stage_alloc >= 3;
     int stages = static_cast<int>((pair ? kSwapPairRing : kSwapSmemBytes) / stage_alloc);
     if (stages > kSwapMaxStages)
         stages = kSwapMaxStages;
-
-    // 5-D map over the seq buffer: {d, Hp, P, Np, P*B}
-    const uint8_t *seq = static_cast<const uint8_t *>(to_head ? src : dst);
-    CUtensorMap map;
-    const CUtensorMapDataType dt = esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32;
-    cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hp), static_cast<cuuint64_t>(P),
-                          static_cast<cuuint64_t>(Np), static_cast<cuuint64_t>(P) * static_cast<cuuint64_t>(B)};
-    cuuint64_t strides[4] = {static_cast<cuuint64_t>(d) * esize, static_cast<cuuint64_t>(row_bytes),
-                             static_cast<cuuint64_t>(H) * d * esize,
-                             static_cast<cuuint64_t>(Np) * H * d * esize};
-    cuuint32_t box[5] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(Hp), 1, static_cast<cuuint32_t>(T), 1};
-    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult cr = tensor_map_encoder()(&map, dt, 5, const_cast<uint8_t *>(seq), dims, strides, box, estr,
-                                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-
-    SwapParams p;
-    p.head = static_cast<uint8_t *>(to_head ? dst : const_cast<void *>(src));
-    p.B = B;
-    p.N = N;
-    p.Np = Np;
-    p.P = P;
-    p.row_bytes = row_bytes;
-    p.T = T;
-    p.nchunks = (Np + T - 1) / T;
-    p.nitems = static_cast<int64_t>(P) * B * p.nchunks * P;
     p.stages = stages;
-    p.stage_bytes = stage_bytes;
-    p.w = wait_cfg();
+    p.stage_alloc = stage_alloc;
 
-    const size_t smem = static_cast<size_t>(stages) * ((stage_bytes + 1023) & ~1023u) + 1024;
+    const size_t smem = static_cast<size_t>(stages) * stage_alloc + 1024;
     int64_t grid = (pair ? 2 : 1) * static_cast<int64_t>(num_sms());
     if (grid > p.nitems)
         grid = p.nitems;
-    cudaError_t e;
-    if (to_head) {
-        e = cudaFuncSetAttribute(swap_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        swap_kernel<true><<<static_cast<unsigned>(grid), 32, smem, stream>>>(map, p);
-    } else {
-        e = cudaFuncSetAttribute(swap_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        swap_kernel<false><<<static_cast<unsigned>(grid), 32, smem, stream>>>(map, p);
-    }
+    cudaError_t e = cudaFuncSetAttribute(swap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    swap_kernel<<<static_cast<unsigned>(grid), 32, smem, stream>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_swap(bool to_head, const void *src, void *dst, int64_t B, int64_t N, int H, int d, int P,
+                        int esize, cudaStream_t stream)
+{
+    SwapDesc one{src, dst, H, to_head ? 1 : 0};
+    return launch_swap_batch(&one, 1, B, N, d, P, esize, stream);
 }
 
 }  // namespace uly

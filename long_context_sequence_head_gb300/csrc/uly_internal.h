@@ -57,6 +57,18 @@ inline WaitCfg wait_cfg() { return WaitCfg{device_status_ptr(), wait_limit_ns()}
 cudaError_t launch_swap(bool to_head, const void *src, void *dst, int64_t B, int64_t N, int H, int d, int P,
                         int esize, cudaStream_t stream);
 
+// Up to kSwapMaxBatch tensors with common B, N, d, P and element size in one
+// launch; each has its own head count and direction.
+constexpr int kSwapMaxBatch = 4;
+struct SwapDesc {
+    const void *src;
+    void *dst;
+    int H;
+    int to_head;
+};
+cudaError_t launch_swap_batch(const SwapDesc *descs, int n, int64_t B, int64_t N, int d, int P, int esize,
+                              cudaStream_t stream);
+
 // ----------------------------------------------------------- attention
 // Where the rows of an attention tensor live.
 //   head layout (seq == 0): [S][B][N][H][d], shard-major, what the swap writes;

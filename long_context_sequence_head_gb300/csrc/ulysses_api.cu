@@ -232,6 +232,39 @@ uly_status ulysses_head_to_seq(const void *x_head, void *x_seq, int64_t B, int64
                                       static_cast<cudaStream_t>(stream)));
 }
 
+uly_status ulysses_swap_batch(const uly_swap_desc *descs_host, int32_t n_descs, int64_t B, int64_t N, int32_t d,
+                              int32_t P, uly_dtype dtype, void *stream)
+{
+    if (descs_host == nullptr || n_descs < 1 || n_descs > uly::kSwapMaxBatch)
+        return ULY_ERR_INVALID_ARG;
+    uly::SwapDesc descs[uly::kSwapMaxBatch];
+    const int es = esize_of(dtype);
+    for (int i = 0; i < n_descs; ++i) {
+        const uly_swap_desc &x = descs_host[i];
+        if (x.to_head != 0 && x.to_head != 1)
+            return ULY_ERR_INVALID_ARG;
+        const uly_status st = check_swap_args(x.src, x.dst, B, N, x.H, d, P, dtype);
+        if (st != ULY_OK)
+            return st;
+        descs[i] = uly::SwapDesc{x.src, x.dst, x.H, x.to_head};
+    }
+    // the entries run concurrently: no entry may write where another reads or writes
+    for (int i = 0; i < n_descs; ++i) {
+        const size_t bi = static_cast<size_t>(B) * N * descs_host[i].H * d * es;
+        for (int j = 0; j < n_descs; ++j) {
+            if (i == j)
+                continue;
+            const size_t bj = static_cast<size_t>(B) * N * descs_host[j].H * d * es;
+            if (overlap(descs_host[i].dst, bi, descs_host[j].src, bj) ||
+                overlap(descs_host[i].dst, bi, descs_host[j].dst, bj))
+                return ULY_ERR_OVERLAP;
+        }
+    }
+    if (uly::tensor_map_encoder() == nullptr || uly::device_status_ptr() == nullptr)
+        return ULY_ERR_CUDA;
+    return from_cuda(uly::launch_swap_batch(descs, n_descs, B, N, d, P, es, static_cast<cudaStream_t>(stream)));
+}
+
 size_t ulysses_attn_workspace_size(int64_t B, int64_t N, int32_t Hq_local, int32_t Hkv_local, int32_t d,
                                    int32_t num_shards, int32_t num_docs, int32_t for_bwd, uly_dtype dtype)
 {

@@ -54,6 +54,27 @@ def test_swap_validation(uly):
     assert _swap(lib, a, b, 1, 8, 4, 64, 2, dt=7) == INVALID
 
 
+def _batch(lib, uly, entries, B, N, d, P, dt=BF16):
+    descs = (uly._SwapDesc * max(len(entries), 1))()
+    for i, (src, dst, H, to_head) in enumerate(entries):
+        descs[i] = uly._SwapDesc(src, dst, H, to_head)
+    return lib.ulysses_swap_batch(ctypes.cast(descs, ctypes.c_void_p), len(entries), B, N, d, P, dt, None)
+
+
+def test_swap_batch_validation(uly):
+    lib = uly.load()
+    a, b, c, e = 1 << 20, 1 << 40, 1 << 41, 1 << 42  # never dereferenced
+    assert lib.ulysses_swap_batch(None, 1, 1, 8, 64, 2, BF16, None) == INVALID
+    assert _batch(lib, uly, [], 1, 8, 64, 2) == INVALID                                  # empty batch
+    assert _batch(lib, uly, [(a, b, 4, 1)] * 5, 1, 8, 64, 2) == INVALID                  # more than four
+    assert _batch(lib, uly, [(a, b, 4, 1), (c, e, 6, 1)], 1, 8, 64, 4) == INVALID        # 6 heads, P = 4
+    assert _batch(lib, uly, [(a, b, 4, 2)], 1, 8, 64, 2) == INVALID                      # direction flag
+    assert _batch(lib, uly, [(a, b, 4, 1), (c + 8, e, 4, 0)], 1, 8, 64, 2) == MISALIGNED
+    assert _batch(lib, uly, [(a, b, 4, 1), (c, b, 4, 1)], 1, 8, 64, 2) == OVERLAP        # two writers
+    assert _batch(lib, uly, [(a, b, 4, 1), (b, c, 4, 0)], 1, 8, 64, 2) == OVERLAP        # one reads the other's output
+    assert _batch(lib, uly, [(a, b, 4, 1), (c, e, 4, 1)], 1, 8, 96, 2) == UNSUPPORTED    # head_dim
+
+
 def test_head_divisibility_golden(uly):
     """32 heads support SP sizes 1, 2, 4, 8, 16, 32 (fixture cites the page)."""
     lib = uly.load()

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from parity_utils import bytes_equal
+from parity_utils import Guards, bytes_equal
 from ulysses_inputs import WORKLOADS, draw_seq_inputs
 
 pytestmark = pytest.mark.gpu
@@ -25,15 +25,17 @@ def test_swap_bit_exact(uly, oracle_mod, dtype, P, B, N, H, d):
     g = torch.Generator().manual_seed(N + H)
     x = torch.randn(P, B, N // P, H, d, generator=g).to(dtype)
     xd = x.cuda()
-    h = torch.full((P, B, N, H // P, d), float("nan"), dtype=dtype, device="cuda")
+    g = Guards()
+    h = g.empty((P, B, N, H // P, d), dtype, float("nan"))
     uly.ulysses_seq_to_head(xd, h, P)
     ref = oracle_mod.seq_to_head(x, P)
     assert bytes_equal(h, ref)
-    back = torch.full_like(xd, float("nan"))
+    back = g.full_like(xd, float("nan"))
     uly.ulysses_head_to_seq(h, back, P)
     assert bytes_equal(back, x)
     st, site = uly.ulysses_get_device_status()
     assert st == 0, hex(site)
+    g.check()
 
 
 @pytest.mark.parametrize("name", ["qwen3_4b_n65536", "single_shard_n1m"])
@@ -52,3 +54,37 @@ def test_swap_full_size(uly, oracle_mod, name):
         assert torch.equal(back.view(torch.int16), x.view(torch.int16))
         del h, back, ref
     assert uly.ulysses_get_device_status()[0] == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("P,B,N,Hq,Hkv,d", [
+    (4, 1, 8192, 32, 8, 128),   # Q, K, V of the Qwen3-4B shapes
+    (4, 2, 1000, 8, 4, 128),    # ragged: 250 tokens per shard, two batches
+    (2, 1, 256, 4, 4, 64),      # the fp32 workload's shape
+    (8, 1, 8 * 37, 8, 8, 64),   # one head per rank, odd chunk
+])
+def test_swap_batch_bit_exact(uly, oracle_mod, dtype, P, B, N, Hq, Hkv, d):
+    """Q, K, V to the head layout in one launch, then O back while dO comes in
+    (two directions in one launch), then dQ, dK, dV back: every tensor equals
+    the oracle's index map bit for bit, and nothing is written outside it."""
+    g = torch.Generator().manual_seed(N + Hq + Hkv)
+    seqs = {n: torch.randn(P, B, N // P, H, d, generator=g).to(dtype)
+            for n, H in (("q", Hq), ("k", Hkv), ("v", Hkv), ("dout", Hq))}
+    dev = {n: x.cuda() for n, x in seqs.items()}
+    G = Guards()
+    heads = {n: G.empty((P, B, N, x.shape[3] // P, d), dtype, float("nan")) for n, x in seqs.items()}
+    uly.ulysses_swap_batch([(dev[n], heads[n], True) for n in ("q", "k", "v")], P)
+    for n in ("q", "k", "v"):
+        assert bytes_equal(heads[n], oracle_mod.seq_to_head(seqs[n], P)), n
+    # O back (here: the head-layout Q stands in for O) while dO comes in
+    o_seq = G.full_like(dev["q"], float("nan"))
+    uly.ulysses_swap_batch([(heads["q"], o_seq, False), (dev["dout"], heads["dout"], True)], P)
+    assert bytes_equal(o_seq, seqs["q"])
+    assert bytes_equal(heads["dout"], oracle_mod.seq_to_head(seqs["dout"], P))
+    back = {n: G.full_like(dev[n], float("nan")) for n in ("q", "k", "v")}
+    uly.ulysses_swap_batch([(heads[n], back[n], False) for n in ("q", "k", "v")], P)
+    for n in ("q", "k", "v"):
+        assert bytes_equal(back[n], seqs[n]), n
+    st, site = uly.ulysses_get_device_status()
+    assert st == 0, hex(site)
+    G.check()
