@@ -66,6 +66,18 @@ def _workload(name, seq_len=None):
     return w, cu
 
 
+def _config(w, args, world):
+    """The workload description both arms print (the same keys and values, so
+    that the two lines can be matched)."""
+    es = 2 if w.dtype == "bf16" else 4
+    in_bytes = w.P * w.B * (w.N // w.P) * (2 * w.Hq + 2 * w.Hkv) * w.d * es
+    return {"workload": args.workload + (f" (N overridden to {w.N})" if args.seq_len else ""), "B": w.B,
+            "N": w.N, "P": w.P, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "causal": w.causal,
+            "head_shards_timed": w.shards_timed, "packed_docs": w.packed_docs,
+            "l2": "no flush: inputs larger than L2 (Q,K,V,dO %.2f GiB per step)" % (in_bytes / 2**30),
+            "parallelism": f"replicas x{world} (virtual P={w.P} inside each GPU)"}
+
+
 def _flops(w, cu):
     fwd = 4.0 * w.d * (w.Hp * w.shards_timed) * w.B * _pairs(w.N, cu)
     return fwd, 2.5 * fwd
@@ -205,98 +217,164 @@ def pipelined_steps(n_steps, stream, up, down, step, sets_in, sets_out, result_o
     return e0, e1
 
 
+class Layer:
+    """Device buffers and the step of one workload: the seq-layout inputs,
+    the head-layout working tensors, the seq-layout outputs and the
+    attention workspaces, all resident in HBM."""
+
+    def __init__(self, uly, w, cu, dev, seed):
+        import torch
+        from ulysses_inputs import draw_seq_inputs
+        self.uly, self.w, self.cu, self.dev = uly, w, cu, dev
+        P, S, B, N, d = w.P, w.shards_timed, w.B, w.N, w.d
+        seq = draw_seq_inputs(w, seed=seed, device="cuda")
+        self.ins = (seq["q"], seq["k"], seq["v"], seq["dout"])
+        bt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        E = lambda *s: torch.empty(*s, dtype=bt, device=dev)
+        self.qh, self.kh, self.vh, self.doh = (E(P, B, N, w.Hp, d), E(P, B, N, w.Hkvp, d), E(P, B, N, w.Hkvp, d),
+                                               E(P, B, N, w.Hp, d))
+        self.oh, self.dqh, self.dkh, self.dvh = (E(S, B, N, w.Hp, d), E(S, B, N, w.Hp, d), E(S, B, N, w.Hkvp, d),
+                                                 E(S, B, N, w.Hkvp, d))
+        self.lse = torch.empty(S, B, w.Hp, N, dtype=torch.float32, device=dev)
+        self.outs = (E(P, B, N // P, w.Hq, d), E(P, B, N // P, w.Hq, d), E(P, B, N // P, w.Hkv, d),
+                     E(P, B, N // P, w.Hkv, d))
+        nd = 0 if cu is None else len(cu) - 1
+        self.ws_f = torch.empty(uly.ulysses_attn_workspace_size(B, N, w.Hp, w.Hkvp, d, S, nd, False, bt),
+                                dtype=torch.uint8, device=dev)
+        self.ws_b = torch.empty(uly.ulysses_attn_workspace_size(B, N, w.Hp, w.Hkvp, d, S, nd, True, bt),
+                                dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream()
+        # the 1M workload times one head shard; the swaps back need all shards
+        self.full = S == P
+
+    @property
+    def launches_per_step(self) -> int:
+        # swaps: Q/K/V in one launch, O back with dO in, dQ/dK/dV back (dO alone
+        # when only some shards are timed); forward 1; backward 3 (pre-pass,
+        # main, dQ conversion)
+        return (3 if self.full else 2) + 1 + 3
+
+    def step(self, ev=None, ins=None, outs_seq=None, after_o=None, before_do=None):
+        """One layer step on the inputs `ins` = (q, k, v, dO) in the seq layout,
+        writing (O, dQ, dK, dV) in the seq layout to `outs_seq`.  `after_o` is
+        called once O is final, `before_do` before dO is first read."""
+        uly, w, cu, P, S = self.uly, self.w, self.cu, self.w.P, self.w.shards_timed
+        q, k, v, do = ins if ins is not None else self.ins
+        o_seq, dq_seq, dk_seq, dv_seq = outs_seq if outs_seq is not None else self.outs
+        qh, kh, vh, doh, oh, dqh, dkh, dvh = (self.qh, self.kh, self.vh, self.doh, self.oh, self.dqh, self.dkh,
+                                              self.dvh)
+
+        def mark(i):
+            if ev is not None:
+                ev[i].record(self.stream)
+        mark(0)
+        uly.ulysses_swap_batch([(q, qh, True), (k, kh, True), (v, vh, True)], P)
+        mark(1)
+        uly.ulysses_attn_fwd(qh[:S], kh[:S], vh[:S], oh, self.lse, causal=w.causal, cu_seqlens=cu,
+                             workspace=self.ws_f)
+        mark(2)
+        if before_do is not None:
+            before_do()
+        if self.full:
+            uly.ulysses_swap_batch([(oh, o_seq, False), (do, doh, True)], P)
+        else:
+            uly.ulysses_seq_to_head(do, doh, P)
+        if after_o is not None:
+            after_o()
+        mark(3)
+        uly.ulysses_attn_bwd(qh[:S], kh[:S], vh[:S], oh, self.lse, doh[:S], dqh, dkh, dvh, causal=w.causal,
+                             cu_seqlens=cu, workspace=self.ws_b)
+        mark(4)
+        if self.full:
+            uly.ulysses_swap_batch([(dqh, dq_seq, False), (dkh, dk_seq, False), (dvh, dv_seq, False)], P)
+        mark(5)
+
+    def swap_bytes(self) -> int:
+        b = 2 * sum(x.numel() * x.element_size() for x in self.ins)
+        if self.full:
+            b += 2 * sum(x.numel() * x.element_size() for x in (self.oh, self.dqh, self.dkh, self.dvh))
+        return b
+
+    def time(self, steps, warmup, barrier, check):
+        """Warm-up, then `steps` timed steps between barriers; returns the
+        elapsed device ms and the mean ms of the five phases."""
+        import torch
+        for _ in range(warmup):
+            self.step()
+        barrier()
+        check("after warm-up")
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        t0.record(self.stream)
+        for i in range(steps):
+            self.step(evs[i])
+        t1.record(self.stream)
+        barrier()
+        check("in the timed region")
+        phase = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(steps)]
+        return t0.elapsed_time(t1), [statistics.mean(p[j] for p in phase) for j in range(5)]
+
+
+def _rates(w, cu, layer, ms, ph, tc_sus, hbm):
+    fwd_flops, bwd_flops = _flops(w, cu)
+    step_flops = fwd_flops + bwd_flops
+    swap_ms = ph[0] + ph[2] + ph[4]  # phases 0, 2 and 4 hold every swap
+    sb = layer.swap_bytes() if layer.full else 2 * sum(
+        x.numel() * x.element_size() for x in layer.ins)
+    fb = step_flops / ((ph[1] + ph[3]) * 1e-3) / 1e12
+    return {
+        "ms_per_step": round(ms, 3), "value": round(step_flops / (ms * 1e-3) / 1e12, 2),
+        "tokens_per_s": round(w.B * w.N / (ms * 1e-3), 1),
+        "attn_fwd_tflops": round(fwd_flops / (ph[1] * 1e-3) / 1e12, 1),
+        "attn_bwd_tflops": round(bwd_flops / (ph[3] * 1e-3) / 1e12, 1),
+        "attn_fwd_bwd_tflops": round(fb, 1), "attn_fwd_bwd_frac_of_bf16_peak": round(fb / tc_sus, 3),
+        "swap_gbps": round(sb / (swap_ms * 1e-3) / 1e9, 1),
+        "swap_frac_of_hbm": round(sb / (swap_ms * 1e-3) / 1e9 / hbm, 3),
+        "phase_ms": {"swap_qkv": round(ph[0], 3), "attn_fwd": round(ph[1], 3),
+                     "swap_o_and_do": round(ph[2], 3), "attn_bwd": round(ph[3], 3),
+                     "swap_dq_dk_dv": round(ph[4], 3)}}
+
+
+# the other workloads timed beside the headline one: (name, steps, warm-up)
+OTHER_WORKLOADS = (("qwen3_4b_n8192", 10, 3), ("packed_docs_n32768", 10, 3), ("tiny_fp32_n256", 10, 3),
+                   ("single_shard_n1m", 1, 1))
+
+
 def run_ours(args, rank, world, dist):
     import torch
     import long_context_sequence_head_gb300 as uly
-    from ulysses_inputs import draw_seq_inputs
 
     uly.load(build_if_missing=True)
     w, cu = _workload(args.workload, args.seq_len)
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     P, S, B, N, d = w.P, w.shards_timed, w.B, w.N, w.d
-    seq = draw_seq_inputs(w, seed=args.seed + rank, device="cuda")
-    q, k, v, do = seq["q"], seq["k"], seq["v"], seq["dout"]
-    bt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-    E = lambda *s: torch.empty(*s, dtype=bt, device=dev)
-    qh, kh, vh, doh = E(P, B, N, w.Hp, d), E(P, B, N, w.Hkvp, d), E(P, B, N, w.Hkvp, d), E(P, B, N, w.Hp, d)
-    oh, dqh, dkh, dvh = E(S, B, N, w.Hp, d), E(S, B, N, w.Hp, d), E(S, B, N, w.Hkvp, d), E(S, B, N, w.Hkvp, d)
-    lse = torch.empty(S, B, w.Hp, N, dtype=torch.float32, device=dev)
-    o_seq, dq_seq = E(P, B, N // P, w.Hq, d), E(P, B, N // P, w.Hq, d)
-    dk_seq, dv_seq = E(P, B, N // P, w.Hkv, d), E(P, B, N // P, w.Hkv, d)
-    nd = 0 if cu is None else len(cu) - 1
-    ws_f = torch.empty(uly.ulysses_attn_workspace_size(B, N, w.Hp, w.Hkvp, d, S, nd, False, bt),
-                       dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(uly.ulysses_attn_workspace_size(B, N, w.Hp, w.Hkvp, d, S, nd, True, bt),
-                       dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-    full = S == P  # the 1M workload times one head shard; swaps back then need all shards
-    q_in, k_in, v_in, do_in = q, k, v, do
-    outs_main = (o_seq, dq_seq, dk_seq, dv_seq)
-
-    def step(ev=None, ins=None, outs_seq=None, after_o=None, before_do=None):
-        """One layer step on the inputs `ins` = (q, k, v, dO) in the seq layout,
-        writing (O, dQ, dK, dV) in the seq layout to `outs_seq`.  `after_o` is
-        called once O is final, `before_do` before dO is first read."""
-        q, k, v, do = ins if ins is not None else (q_in, k_in, v_in, do_in)
-        o_seq, dq_seq, dk_seq, dv_seq = outs_seq if outs_seq is not None else outs_main
-
-        def mark(i):
-            if ev is not None:
-                ev[i].record(stream)
-        mark(0)
-        uly.ulysses_seq_to_head(q, qh, P)
-        uly.ulysses_seq_to_head(k, kh, P)
-        uly.ulysses_seq_to_head(v, vh, P)
-        mark(1)
-        uly.ulysses_attn_fwd(qh[:S], kh[:S], vh[:S], oh, lse, causal=w.causal, cu_seqlens=cu, workspace=ws_f)
-        mark(2)
-        if full:
-            uly.ulysses_head_to_seq(oh, o_seq, P)
-        if after_o is not None:
-            after_o()
-        if before_do is not None:
-            before_do()
-        uly.ulysses_seq_to_head(do, doh, P)
-        mark(3)
-        uly.ulysses_attn_bwd(qh[:S], kh[:S], vh[:S], oh, lse, doh[:S], dqh, dkh, dvh, causal=w.causal,
-                             cu_seqlens=cu, workspace=ws_b)
-        mark(4)
-        if full:
-            uly.ulysses_head_to_seq(dqh, dq_seq, P)
-            uly.ulysses_head_to_seq(dkh, dk_seq, P)
-            uly.ulysses_head_to_seq(dvh, dv_seq, P)
-        mark(5)
+    layer = Layer(uly, w, cu, dev, args.seed + rank)
+    q, k, v, do = layer.ins
+    bt = q.dtype
+    o_seq, dq_seq, dk_seq, dv_seq = layer.outs
+    oh, dqh, dkh, dvh, lse = layer.oh, layer.dqh, layer.dkh, layer.dvh, layer.lse
+    ws_f, ws_b = layer.ws_f, layer.ws_b
+    stream = layer.stream
+    full = layer.full
+    outs_main = layer.outs
+    step = layer.step
 
     def barrier():
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    st, site = uly.ulysses_get_device_status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} at site {site:#x} after warm-up")
+    def check(where):
+        st, site = uly.ulysses_get_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} at site {site:#x} {where}")
 
     # ---- timed region: device time, inputs resident in HBM
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     with ClockSampler(dev.index, args.clock_log_dir) as clk:
-        barrier()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for i in range(args.steps):
-            step(evs[i])
-        t1.record(stream)
-        barrier()
-    elapsed_ms = t0.elapsed_time(t1)
-    st, site = uly.ulysses_get_device_status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} at site {site:#x} in the timed region")
-    phase = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(args.steps)]
-    ph = [statistics.mean(p[j] for p in phase) for j in range(5)]
+        elapsed_ms, ph = layer.time(args.steps, args.warmup, barrier, check)
     elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
 
     # ---- the same step through the fused seq-layout calls (no swaps)
@@ -458,9 +536,7 @@ def run_ours(args, rank, world, dist):
     ms = elapsed_ms / args.steps
     value = whole_job_throughput(world, step_flops, ms)
     hbm, tc_burst, tc_sus, src = _peaks()
-    swap_bytes = 2 * sum(x.numel() * x.element_size() for x in (q, k, v, do))
-    if full:
-        swap_bytes += 2 * sum(x.numel() * x.element_size() for x in (oh, dqh, dkh, dvh))
+    swap_bytes = layer.swap_bytes()
     # phases 0, 2 and 4 hold every swap (2 = O back to seq + dO to head)
     swap_ms = ph[0] + ph[2] + ph[4]
     bwd_tflops = bwd_flops / (ph[3] * 1e-3) / 1e12
@@ -481,11 +557,7 @@ def run_ours(args, rank, world, dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded N(0,1) Q/K/V/dO of the workload's shapes)",
-        "config": {"workload": args.workload + (f" (N overridden to {N})" if args.seq_len else ""), "B": B, "N": N, "P": P, "Hq": w.Hq, "Hkv": w.Hkv, "d": d,
-                   "causal": w.causal, "head_shards_timed": S, "packed_docs": w.packed_docs,
-                   "l2": "no flush: inputs larger than L2 (Q,K,V,dO %.2f GiB per step)" % (
-                       sum(x.numel() * x.element_size() for x in (q, k, v, do)) / 2**30),
-                   "parallelism": f"replicas x{world} (virtual P={P} inside each GPU)"},
+        "config": _config(w, args, world),
         "tokens_per_s": round(world * B * N / (ms * 1e-3), 1),
         "attn_fwd_tflops": round(fwd_tflops, 1), "attn_bwd_tflops": round(bwd_tflops, 1),
         "attn_fwd_bwd_tflops": round(step_flops / ((ph[1] + ph[3]) * 1e-3) / 1e12, 1),
@@ -521,19 +593,109 @@ def run_ours(args, rank, world, dist):
             "comm_model_bytes_per_gpu_per_layer": ring["comm_model_bytes_per_gpu"]},
         "sharded_loss": loss,
         "clocks": clk.summary(),
-        "gpu_launches": args.steps * ((8 if full else 4) + 1 + 3),
+        "gpu_launches": args.steps * layer.launches_per_step,
     }
     return line
 
 
 # ------------------------------------------------------------ oracle arm
-def oracle_inputs(w, seed):
+def oracle_inputs(w, seed, want_dout=True, device="cpu"):
     """The workload's inputs in the oracle's head layout, upcast to fp64 once
-    (outside any timed region)."""
+    (outside any timed region).  device="cuda" draws them with the seeded
+    generator on the GPU (the bytes the GPU arm times, and fast for the 1M
+    workload) before they are copied to the host."""
     import oracle
     from ulysses_inputs import draw_seq_inputs
-    seq = draw_seq_inputs(w, seed=seed, device="cpu")
-    return {n: oracle._f64(oracle.seq_to_head(seq[n], w.P)[: w.shards_timed]) for n in seq}
+    seq = draw_seq_inputs(w, seed=seed, device=device, want_dout=want_dout)
+    out = {}
+    for n in list(seq):
+        x = seq.pop(n).cpu()
+        out[n] = oracle._f64(oracle.seq_to_head(x, w.P)[: w.shards_timed])
+        del x
+    return out
+
+
+def oracle_workload_baseline(w, cu, seed):
+    """The fp64 oracle, as it stands, on a bounded sample of one workload
+    (a few seconds of host work): the whole forward and backward for the
+    tiny workload, random query rows (forward + dQ) for the N=8192 and
+    packed-document workloads, and 256 random forward rows (O, lse) of the
+    one timed head shard for the 1M workload.  Credited FLOPs: the step's
+    algorithmic FLOPs for the full case; 4*d per allowed pair for a forward
+    row and 6*d for a dQ row."""
+    import numpy as np
+    import oracle
+    heads = oracle_inputs(w, seed, want_dout=w.N < (1 << 20), device="cuda")
+    rng = np.random.default_rng(seed)
+    S = w.shards_timed
+
+    def allowed(i):
+        if cu is None:
+            return i + 1
+        kk = int(np.searchsorted(cu, i, side="right")) - 1
+        return i - int(cu[kk]) + 1
+    if w.N <= 1024:
+        fwd, bwd = _flops(w, cu)
+        reps = 0
+        t0 = time.perf_counter()
+        while reps == 0 or time.perf_counter() - t0 < 1.0:
+            oracle.attn_bwd(heads["q"], heads["k"], heads["v"], heads["dout"], causal=w.causal, cu_seqlens=cu)
+            reps += 1
+        dt = time.perf_counter() - t0
+        credit = reps * (fwd + bwd)
+        sample = f"the whole forward and backward of {w.name} (all {S} head shards), {reps} times"
+    elif w.N < (1 << 20):
+        rows = [(int(rng.integers(S)), 0, int(rng.integers(w.Hp)), int(rng.integers(w.N))) for _ in range(8192)]
+        credit = sum(10 * w.d * allowed(i) for *_, i in rows)
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(heads["q"], heads["k"], heads["v"], rows, cu_seqlens=cu)
+        oracle.attn_bwd_q_rows(heads["q"], heads["k"], heads["v"], heads["dout"], rows, cu_seqlens=cu)
+        dt = time.perf_counter() - t0
+        sample = f"8192 random query rows (forward + dQ) of {w.name}"
+    else:
+        rows = [(0, 0, int(rng.integers(w.Hp)), int(rng.integers(w.N))) for _ in range(256)]
+        credit = sum(4 * w.d * allowed(i) for *_, i in rows)
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(heads["q"], heads["k"], heads["v"], rows, cu_seqlens=cu)
+        dt = time.perf_counter() - t0
+        sample = f"256 random forward rows (O, lse) of the timed head shard of {w.name}"
+    return {"value": credit / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": sample, "seconds": round(dt, 2)}
+
+
+def run_other_workloads(args, with_cpu_baseline):
+    """The configurations beside the headline one, each timed on the same
+    step (swaps, forward, backward) with its own warm-up, and, on request,
+    the oracle timed on a bounded sample of it."""
+    import argparse as _ap
+    import torch
+    import long_context_sequence_head_gb300 as uly
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    hbm, _, tc_sus, _ = _peaks()
+
+    def barrier():
+        torch.cuda.synchronize()
+
+    def check(where):
+        st, site = uly.ulysses_get_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} at site {site:#x} {where}")
+    out = {}
+    for name, steps, warmup in OTHER_WORKLOADS:
+        w, cu = _workload(name)
+        torch.cuda.empty_cache()
+        layer = Layer(uly, w, cu, dev, args.seed)
+        total_ms, ph = layer.time(steps, warmup, barrier, check)
+        r = _rates(w, cu, layer, total_ms / steps, ph, tc_sus, hbm)
+        r.update({"steps": steps, "warmup": warmup, "dtype": w.dtype,
+                  "config": _config(w, _ap.Namespace(workload=name, seq_len=None), 1),
+                  "gpu_launches": steps * layer.launches_per_step})
+        del layer
+        torch.cuda.empty_cache()
+        if with_cpu_baseline:
+            r["cpu_baseline"] = oracle_workload_baseline(w, cu, args.seed)
+        out[name] = r
+    return out
 
 
 def oracle_sample(w, cu, heads, rows_per_step, seed):
@@ -581,8 +743,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.workload, "N": w.N, "P": w.P, "Hq": w.Hq,
-                                        "Hkv": w.Hkv, "d": w.d},
+        "data": "synthetic (seeded N(0,1) Q/K/V/dO of the workload's shapes)", "config": _config(w, args, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"per step: {sample}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -606,6 +767,8 @@ def main():
     ap.add_argument("--no-loss", action="store_true", help="skip the sequence-parallel loss measurement")
     ap.add_argument("--no-ring", action="store_true", help="skip the ring-attention measurement")
     ap.add_argument("--vocab", type=int, default=151936, help="vocabulary of the loss measurement (Qwen3)")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="time only the headline workload (skip the N=8192, packed, tiny and 1M lines)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -623,6 +786,8 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
     line = run_ours(args, rank, world, dist)
+    if world == 1 and not args.no_other_workloads and args.seq_len is None:
+        line["other_workloads"] = run_other_workloads(args, with_cpu_baseline=not args.no_cpu_baseline)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         w, cu = _workload(args.workload, args.seq_len)
         import oracle

@@ -29,6 +29,13 @@ def test_reference_arm_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
     assert d["value"] > 0 and d["higher_is_better"] is True and d["vs_baseline"] is None
     assert d["config"]["workload"] == "qwen3_4b_n8192"
+    # the same config keys and values as the GPU arm prints for this workload
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    from ulysses_inputs import WORKLOADS
+    args = argparse.Namespace(workload="qwen3_4b_n8192", seq_len=None)
+    assert d["config"] == bench._config(WORKLOADS["qwen3_4b_n8192"], args, 1)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["unit"] == d["unit"]
     e2e = d["e2e"]
