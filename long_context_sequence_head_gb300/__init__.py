@@ -232,6 +232,86 @@ def ulysses_swap_batch(items, P: int, stream=None):
         else ULY_FP32, _stream(stream)))
 
 
+# ------------------------------------------------ all-to-all across GPUs
+
+def _a2a_shapes(x, P, what):
+    if x.dim() != 4 or x.shape[0] != 1:
+        raise ValueError(f"{what} must be [1][tokens][heads][d] (batch 1), got {tuple(x.shape)}")
+    return x.shape[1], x.shape[2], x.shape[3]
+
+
+def ulysses_a2a_pack(x_local: torch.Tensor, P: int, out: Optional[torch.Tensor] = None, stream=None):
+    """Send buffer of the seq->head all-to-all on one rank: this rank's
+    sequence shard x_local [1][T][H][d] (its T tokens, all H heads) as P
+    contiguous blocks [P][1][T][H/P][d], block s holding head block s for
+    rank s.  It is the library's seq->head kernel applied to the rank's own
+    shard seen as P sub-shards of T/P tokens (so T % P == 0)."""
+    T, H, d = _a2a_shapes(x_local, P, "x_local")
+    if T % P or H % P:
+        raise ValueError(f"the local tokens ({T}) and the heads ({H}) must be multiples of P={P}")
+    if out is None:
+        out = torch.empty(P, 1, T, H // P, d, dtype=x_local.dtype, device=x_local.device)
+    ulysses_seq_to_head(x_local.view(P, 1, T // P, H, d), out, P, stream)
+    return out
+
+
+def ulysses_a2a_unpack(recv: torch.Tensor, P: int, out: Optional[torch.Tensor] = None, stream=None):
+    """Receive side of the head->seq all-to-all on one rank: recv [P][1][T][H/P][d]
+    (block s = head block s of this rank's T tokens, from rank s) back to the
+    sequence shard [1][T][H][d]: the library's head->seq kernel on the rank's
+    own tokens."""
+    Ps, B, T, Hp, d = recv.shape
+    if Ps != P or B != 1 or T % P:
+        raise ValueError(f"recv must be [P={P}][1][T][H/P][d] with T % P == 0, got {tuple(recv.shape)}")
+    if out is None:
+        out = torch.empty(1, T, Hp * P, d, dtype=recv.dtype, device=recv.device)
+    ulysses_head_to_seq(recv, out.view(P, 1, T // P, Hp * P, d), P, stream)
+    return out
+
+
+def ulysses_all_to_all_seq_to_head(x_local: torch.Tensor, group=None, out: Optional[torch.Tensor] = None):
+    """The first all-to-all of Ulysses across the P ranks of a process group
+    (one GPU per rank; Transformers docs "Ulysses sequence parallelism", the
+    all-to-all diagram; blog summary step 3): rank r holds tokens
+    [r*T, (r+1)*T) of all H heads, x_local [1][T][H][d]; afterwards it holds
+    all N = P*T tokens of heads [r*H/P, (r+1)*H/P), returned as the head
+    shard [1][N][H/P][d] that the attention calls take (num_shards = 1).
+
+    The local pack runs in the library's kernel; torch.distributed's
+    all_to_all_single moves block s to rank s, each received block landing in
+    this rank's own buffer.  Blocks arrive in source-rank order, which is
+    token order, so the receive buffer is the head shard with no further
+    copy.  Per rank (P-1)/P of the shard crosses the network: O(N d / P)."""
+    import torch.distributed as dist
+    P = dist.get_world_size(group)
+    T, H, d = _a2a_shapes(x_local, P, "x_local")
+    send = ulysses_a2a_pack(x_local, P)
+    if out is None:
+        out = torch.empty(1, P * T, H // P, d, dtype=x_local.dtype, device=x_local.device)
+    if tuple(out.shape) != (1, P * T, H // P, d) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous [1][{P * T}][{H // P}][{d}] tensor")
+    dist.all_to_all_single(out.view(P, T * (H // P) * d), send.view(P, T * (H // P) * d), group=group)
+    return out
+
+
+def ulysses_all_to_all_head_to_seq(x_head: torch.Tensor, group=None, out: Optional[torch.Tensor] = None):
+    """The second all-to-all (blog summary step 5), the inverse of
+    ulysses_all_to_all_seq_to_head and its backward: this rank's head shard
+    x_head [1][N][H/P][d] in, its sequence shard [1][N/P][H][d] out.  Block s
+    of the head shard (the tokens of rank s) goes to rank s; the P received
+    blocks (head block s of this rank's tokens, from rank s) are put back in
+    the sequence layout by the library's head->seq kernel."""
+    import torch.distributed as dist
+    P = dist.get_world_size(group)
+    N, Hp, d = _a2a_shapes(x_head, P, "x_head")
+    if N % P:
+        raise ValueError(f"the tokens ({N}) must be a multiple of P={P}")
+    T = N // P
+    recv = torch.empty(P, 1, T, Hp, d, dtype=x_head.dtype, device=x_head.device)
+    dist.all_to_all_single(recv.view(P, T * Hp * d), x_head.contiguous().view(P, T * Hp * d), group=group)
+    return ulysses_a2a_unpack(recv, P, out)
+
+
 # -------------------------------------------------------------- attention
 
 def ulysses_attn_workspace_size(B: int, N: int, Hq_local: int, Hkv_local: int, d: int, num_shards: int,
