@@ -53,7 +53,8 @@ typedef enum {
     ULY_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
     ULY_ERR_TIMEOUT = 6,     /* a device-side bounded wait ran out */
     ULY_ERR_WORKSPACE = 7,   /* workspace missing or smaller than required */
-    ULY_ERR_SCRATCH_LIMIT = 8 /* sizes need more scratch than ulysses_attn_bwd_noalloc has */
+    ULY_ERR_SCRATCH_LIMIT = 8, /* sizes need more scratch than ulysses_attn_bwd_noalloc has */
+    ULY_ERR_BOUNDS = 9        /* a bounds check of the debug build failed (see below) */
 } uly_status;
 
 typedef enum { ULY_BF16 = 0, ULY_FP32 = 1 } uly_dtype;
@@ -329,9 +330,12 @@ uly_status ulysses_sharded_ce_loss(const void *logits, const int64_t *labels, vo
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  ULY_OK if no kernel reported a problem since the last read;
  * ULY_ERR_TIMEOUT if a bounded device-side wait ran out (the kernel then
- * stopped early and its outputs are invalid); ULY_ERR_INVALID_ARG if a kernel
- * rejected its launch configuration; ULY_ERR_CUDA on a CUDA error.
- * If site_out is not NULL it receives the id of the first wait that ran out.
+ * stopped early and its outputs are invalid); ULY_ERR_BOUNDS if a kernel of
+ * the debug build found an access outside its buffer (it skipped the access;
+ * outputs are invalid); ULY_ERR_INVALID_ARG if a kernel rejected its launch
+ * configuration; ULY_ERR_CUDA on a CUDA error.  If site_out is not NULL it
+ * receives the id of the first site that reported (a wait, or 0x8000 plus
+ * the id of an access).
  */
 uly_status ulysses_get_device_status(void *stream, uint32_t *site_out);
 
@@ -348,6 +352,16 @@ uly_status ulysses_set_wait_limit_ns(uint64_t limit_ns);
  * tests of the timeout path; it faults nothing and hangs nothing.
  */
 uly_status ulysses_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
+/*
+ * Debug build only (the library compiled with -DULY_DEBUG, which checks every
+ * raw-pointer global access of the swap and attention kernels against its
+ * buffer and reports ULY_ERR_BOUNDS instead of making it): launches one tiny
+ * kernel whose check is given an offset past its extent, touching no memory,
+ * so that the reporting path can be tested.  The release build returns
+ * ULY_ERR_UNSUPPORTED and launches nothing.
+ */
+uly_status ulysses_selftest_bounds(void *stream);
 
 /* Human-readable name of a status code (static string). */
 const char *ulysses_status_string(uly_status status);

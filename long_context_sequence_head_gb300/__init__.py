@@ -28,7 +28,7 @@ ULY_BF16 = 0
 ULY_FP32 = 1
 _STATUS = {0: "ULY_OK", 1: "ULY_ERR_INVALID_ARG", 2: "ULY_ERR_UNSUPPORTED", 3: "ULY_ERR_MISALIGNED",
            4: "ULY_ERR_OVERLAP", 5: "ULY_ERR_CUDA", 6: "ULY_ERR_TIMEOUT", 7: "ULY_ERR_WORKSPACE",
-           8: "ULY_ERR_SCRATCH_LIMIT"}
+           8: "ULY_ERR_SCRATCH_LIMIT", 9: "ULY_ERR_BOUNDS"}
 
 # every symbol include/ulysses.h declares
 EXPORTED = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_swap_batch", "ulysses_attn_workspace_size",
@@ -36,7 +36,7 @@ EXPORTED = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_swap_batch", 
             "ulysses_attn_bwd_noalloc", "ulysses_sharded_ce_workspace_size", "ulysses_sharded_ce_loss",
             "ulysses_ring_attn_workspace_size", "ulysses_ring_attn_fwd", "ulysses_ring_attn_bwd",
             "ulysses_get_device_status",
-            "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout",
+            "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout", "ulysses_selftest_bounds",
             "ulysses_status_string", "ulysses_version")
 
 
@@ -49,8 +49,14 @@ class UlyssesError(RuntimeError):
 _lib = None
 
 
+def debug_build_selected() -> bool:
+    """ULY_DEBUG_BUILD=1 in the environment selects the bounds-checked build
+    of the library (compiled with -DULY_DEBUG) for this process."""
+    return os.environ.get("ULY_DEBUG_BUILD", "") == "1"
+
+
 def library_path() -> str:
-    return _build_mod.SO_PATH
+    return _build_mod.DEBUG_SO_PATH if debug_build_selected() else _build_mod.SO_PATH
 
 
 def load(build_if_missing: bool = False) -> ctypes.CDLL:
@@ -63,7 +69,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         if not build_if_missing:
             raise RuntimeError(f"CUDA library not built: {path} is missing; run "
                                "`python -m long_context_sequence_head_gb300.build`")
-        _build_mod.build()
+        _build_mod.build(debug=debug_build_selected())
     lib = ctypes.CDLL(path)
     i64, i32, u64, vp, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_float
     sz = ctypes.c_size_t
@@ -90,13 +96,15 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.ulysses_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.ulysses_set_wait_limit_ns.argtypes = [u64]
     lib.ulysses_selftest_wait_timeout.argtypes = [u64, vp]
+    lib.ulysses_selftest_bounds.argtypes = [vp]
     lib.ulysses_status_string.argtypes = [i32]
     lib.ulysses_status_string.restype = ctypes.c_char_p
     lib.ulysses_version.restype = i32
     for name in ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_swap_batch", "ulysses_attn_fwd",
                  "ulysses_attn_bwd",
                  "ulysses_attn_bwd_noalloc", "ulysses_attn_fwd_seq", "ulysses_attn_bwd_seq",
-                 "ulysses_get_device_status", "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout"):
+                 "ulysses_get_device_status", "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout",
+                 "ulysses_selftest_bounds"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -532,6 +540,12 @@ def ulysses_set_wait_limit_ns(limit_ns: int) -> None:
 
 def ulysses_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     _check("ulysses_selftest_wait_timeout", load().ulysses_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def ulysses_selftest_bounds(stream=None) -> int:
+    """Debug build: make one bounds check fail without touching memory
+    (returns the call's status; the release build answers ULY_ERR_UNSUPPORTED)."""
+    return int(load().ulysses_selftest_bounds(_stream(stream)))
 
 
 def ulysses_status_string(status: int) -> str:

@@ -5,6 +5,12 @@ sm_103a, ``-lineinfo``), then linked with ``nvcc -shared``.  The CUDA runtime
 is linked statically; the driver's tensor-map encoder is resolved at run time,
 so the library needs no ``-lcuda``.  Run as ``python -m
 long_context_sequence_head_gb300.build`` or through ``__graft_entry__.build()``.
+
+``build(debug=True)`` compiles the same sources with ``-DULY_DEBUG`` into
+``_build/debug/libulysses_gb300_debug.so``: every raw-pointer global access of
+the swap and attention kernels is checked against its buffer and a failure is
+reported as a status (ULY_ERR_BOUNDS) instead of being made.  The binding
+loads it when ULY_DEBUG_BUILD=1.
 """
 from __future__ import annotations
 
@@ -21,6 +27,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 SO_NAME = "libulysses_gb300.so"
 SO_PATH = os.path.join(BUILD, SO_NAME)
+DEBUG_BUILD = os.path.join(BUILD, "debug")
+DEBUG_SO_PATH = os.path.join(DEBUG_BUILD, "libulysses_gb300_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -40,24 +48,27 @@ def _deps():
         os.path.join(ROOT, "include", "ulysses.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(SO_PATH):
+def up_to_date(debug: bool = False) -> bool:
+    so = DEBUG_SO_PATH if debug else SO_PATH
+    if not os.path.exists(so):
         return False
-    t = os.path.getmtime(SO_PATH)
+    t = os.path.getmtime(so)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return SO_PATH
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    so_path = DEBUG_SO_PATH if debug else SO_PATH
+    out_dir = DEBUG_BUILD if debug else BUILD
+    if not force and up_to_date(debug):
+        return so_path
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     common = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
-                     "-I", os.path.join(ROOT, "include"), "-I", CSRC]
+                     "-I", os.path.join(ROOT, "include"), "-I", CSRC] + (["-DULY_DEBUG"] if debug else [])
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc] + common + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,14 +79,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = SO_PATH + f".tmp{os.getpid()}"
+    tmp = so_path + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, SO_PATH)
-    return SO_PATH
+    os.replace(tmp, so_path)
+    return so_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

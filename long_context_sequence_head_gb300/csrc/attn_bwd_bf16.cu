@@ -71,6 +71,7 @@ struct BwdParams {
     const float *Dv;    // [SB][Hq][Npad]
     float *dq_acc;      // [SB][Hq][Npad/128][32][128][4]
     uint16_t *dk, *dv;  // rows like k, v
+    int64_t kv_elems;   // extent of dk, dv (bounds checks of debug builds)
     WaitCfg w;
     RowLayout L;
 };
@@ -111,8 +112,12 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *__restrict
                                                       const uint16_t *__restrict__ dout,
                                                       const float *__restrict__ lse, float *__restrict__ lse2,
                                                       float *__restrict__ Dv, int64_t SB, int64_t N, int64_t Npad,
-                                                      int Hq, RowLayout L)
+                                                      int Hq, RowLayout L, int64_t q_elems, unsigned *status)
 {
+    const int64_t row_elems = SB * Hq * Npad;  // lse2, D
+    (void)q_elems;
+    (void)status;
+    (void)row_elems;
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = lane_id();
     if (gw >= SB * Npad)
@@ -122,12 +127,17 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *__restrict
     if (i >= N) {
         // padded rows: probabilities exactly 0 in the main kernel
         for (int h = lane; h < Hq; h += 32) {
+            if (!ULY_IN_BOUNDS(status, (sb * Hq + h) * Npad + i, 1, row_elems, 0x21))
+                break;
             Dv[(sb * Hq + h) * Npad + i] = 0.f;
             lse2[(sb * Hq + h) * Npad + i] = INFINITY;
         }
         return;
     }
     const int64_t off = L.off(N, sb, i, Hq, 0, kD);
+    // the token's Hq rows are adjacent: one check covers every read below
+    if (!ULY_IN_BOUNDS(status, off, static_cast<int64_t>(Hq) * kD, q_elems, 0x22))
+        return;
     const uint4 *o4 = reinterpret_cast<const uint4 *>(o + off);
     const uint4 *d4 = reinterpret_cast<const uint4 *>(dout + off);
     const int n16 = Hq * (kD / 8);  // 16-byte pieces of the token's rows
@@ -151,8 +161,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *__restrict
         if (u < n16 && (lane & 15) == 0) {
             const int h = u / (kD / 8);
             const int64_t row = (sb * Hq + h) * Npad + i;
-            Dv[row] = acc;
-            lse2[row] = lse[(sb * Hq + h) * N + i] * 1.4426950408889634f;
+            if (ULY_IN_BOUNDS(status, row, 1, row_elems, 0x23) &&
+                ULY_IN_BOUNDS(status, (sb * Hq + h) * N + i, 1, SB * Hq * N, 0x24)) {
+                Dv[row] = acc;
+                lse2[row] = lse[(sb * Hq + h) * N + i] * 1.4426950408889634f;
+            }
         }
     }
 }
@@ -167,8 +180,12 @@ constexpr int kCvtPitch = kD + 4;  // floats per staged row; +4 spreads the grou
 
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc, uint16_t *__restrict__ dq,
                                                          int64_t SB, int64_t N, int64_t Npad, int Hq, float scale,
-                                                         RowLayout L)
+                                                         RowLayout L, int64_t q_elems, unsigned *status)
 {
+    const int64_t acc_elems = SB * Hq * Npad * kD;
+    (void)q_elems;
+    (void)status;
+    (void)acc_elems;
     __shared__ __align__(16) float tile[kCvtRows * kCvtPitch];
     const int64_t ntiles = Npad / kBM;
     int64_t rest = blockIdx.x;
@@ -178,7 +195,11 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
     rest /= ntiles;
     const int h = static_cast<int>(rest % Hq);
     const int64_t sb = rest / Hq;
-    const float *src = acc + ((sb * Hq + h) * ntiles + mt) * (32 * kBM * 4);
+    const int64_t src_off = ((sb * Hq + h) * ntiles + mt) * (32 * kBM * 4);
+    // the tile's whole accumulator block: covers every read below
+    if (!ULY_IN_BOUNDS(status, src_off, 32 * kBM * 4, acc_elems, 0x25))
+        return;
+    const float *src = acc + src_off;
     const int r0 = slab * kCvtRows;
     // consecutive threads take consecutive rows of one column group
     for (int k = threadIdx.x; k < 32 * kCvtRows; k += 256) {
@@ -197,7 +218,9 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
         uint2 out;
         out.x = pack_bf16x2(v.x * scale, v.y * scale);
         out.y = pack_bf16x2(v.z * scale, v.w * scale);
-        *reinterpret_cast<uint2 *>(dq + L.off(N, sb, i, Hq, h, kD) + lane * 4) = out;
+        const int64_t doff = L.off(N, sb, i, Hq, h, kD) + lane * 4;
+        if (ULY_IN_BOUNDS(status, doff, 4, q_elems, 0x26))
+            *reinterpret_cast<uint2 *>(dq + doff) = out;
     }
 }
 
@@ -312,7 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *abort_flag = 1;
                     break;
                 }
-                mbar_expect_tx(&q_full[slot], 2 * kTile + 2 * 512);
+                const int64_t roff = (static_cast<int64_t>(sb) * p.Hq + h) * p.Npad + static_cast<int64_t>(m) * kBM;
+                const bool rows_ok = ULY_IN_BOUNDS(p.w.status, roff, kBM, p.SB * p.Hq * p.Npad, 0x27);
+                mbar_expect_tx(&q_full[slot], 2 * kTile + (rows_ok ? 2 * 512 : 0));
                 uint8_t *sq = smem + BwdSmem::kQ + slot * kTile;
                 uint8_t *sdo = smem + BwdSmem::kdO + slot * kTile;
                 p.L.tile(sb, static_cast<int64_t>(m) * kBM, p.Hq, h, c1, c2, c3, c4);
@@ -320,9 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_5d(sq + kChunk, &tm_q, &q_full[slot], 64, c1, c2, c3, c4);
                 tma_load_5d(sdo, &tm_do, &q_full[slot], 0, c1, c2, c3, c4);
                 tma_load_5d(sdo + kChunk, &tm_do, &q_full[slot], 64, c1, c2, c3, c4);
-                const int64_t roff = (static_cast<int64_t>(sb) * p.Hq + h) * p.Npad + static_cast<int64_t>(m) * kBM;
-                bulk_g2s(smem + BwdSmem::kLse + slot * 512, p.lse2 + roff, 512, &q_full[slot]);
-                bulk_g2s(smem + BwdSmem::kDv + slot * 512, p.Dv + roff, 512, &q_full[slot]);
+                if (rows_ok) {
+                    bulk_g2s(smem + BwdSmem::kLse + slot * 512, p.lse2 + roff, 512, &q_full[slot]);
+                    bulk_g2s(smem + BwdSmem::kDv + slot * 512, p.Dv + roff, 512, &q_full[slot]);
+                }
                 ++issued;
             }
             if (*abort_flag) {
@@ -460,11 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(dq_empty);
-            dq_base = (static_cast<int64_t>(m) * kBM + j < p.N)
-                          ? p.dq_acc +
-                                (((static_cast<int64_t>(sb) * p.Hq + h) * (p.Npad / kBM) + m) * 32 + c0 / 4) *
-                                    (kBM * 4) +
-                                j * 4
+            const int64_t qoff =
+                (((static_cast<int64_t>(sb) * p.Hq + h) * (p.Npad / kBM) + m) * 32 + c0 / 4) * (kBM * 4) + j * 4;
+            // the eight 4-column groups of this row lie in [qoff, qoff + 7 * 128 * 4 + 4)
+            dq_base = (static_cast<int64_t>(m) * kBM + j < p.N &&
+                       ULY_IN_BOUNDS(p.w.status, qoff, 7 * kBM * 4 + 4, p.SB * p.Hq * p.Npad * kD, 0x28))
+                          ? p.dq_acc + qoff
                           : nullptr;
         };
         auto reduce_groups = [&](int g0, int g1) {  // groups g0 .. g1-1 of 8
@@ -586,8 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- dK, dV epilogue: key row j, d columns c0 .. c0+31 ----
         if (mbar_wait_warp(dkv_done, 0, p.w, 0x78) && ok) {
             tc_fence_after();
-            const bool store = key < p.N;
-            const int64_t rowoff = p.L.off(p.N, sb, store ? key : 0, p.Hkv, kvh, kD) + c0;
+            const int64_t rowoff = p.L.off(p.N, sb, key < p.N ? key : 0, p.Hkv, kvh, kD) + c0;
+            const bool store = key < p.N && ULY_IN_BOUNDS(p.w.status, rowoff, 32, p.kv_elems, 0x29);
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 const uint32_t src = (which ? tdK : tdV) + lane_off + c0;
@@ -640,7 +667,7 @@ cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *
         const int64_t blocks = (warps * 32 + 255) / 256;
         bwd_pre_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
             static_cast<const uint16_t *>(o), static_cast<const uint16_t *>(dout), lse, scr.lse2, scr.D, s.SB, s.N,
-            Npad, s.Hq, s.L);
+            Npad, s.Hq, s.L, s.q_elems, s.status);
         e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;
@@ -667,6 +694,7 @@ cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *
     p.dq_acc = scr.dq_acc;
     p.dk = static_cast<uint16_t *>(dk);
     p.dv = static_cast<uint16_t *>(dv);
+    p.kv_elems = s.kv_elems;
     p.w = wait_cfg();
     p.L = s.L;
     {
@@ -700,7 +728,7 @@ cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *
     {
         const int64_t blocks = s.SB * s.Hq * (Npad / kBM) * (kBM / kCvtRows);
         dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            scr.dq_acc, static_cast<uint16_t *>(dq), s.SB, s.N, Npad, s.Hq, s.scale, s.L);
+            scr.dq_acc, static_cast<uint16_t *>(dq), s.SB, s.N, Npad, s.Hq, s.scale, s.L, s.q_elems, s.status);
     }
     return cudaGetLastError();
 }

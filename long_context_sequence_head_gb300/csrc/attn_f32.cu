@@ -59,7 +59,10 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(AttnShape s, const
     if (i >= s.N)
         return;
     const int kvh = h / (s.Hq / s.Hkv);
-    const float *qi = q + s.L.off(s.N, sb, i, s.Hq, h, D);
+    const int64_t qoff = s.L.off(s.N, sb, i, s.Hq, h, D);
+    if (!ULY_IN_BOUNDS(s.status, qoff, D, s.q_elems, 0x01))
+        return;
+    const float *qi = q + qoff;
     float qr[E], acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -72,8 +75,11 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(AttnShape s, const
         hi = i + 1;
     float m = -INFINITY, l = 0.f;
     for (int64_t j = lo; j < hi; ++j) {
-        const float *kj = k + s.L.off(s.N, sb, j, s.Hkv, kvh, D);
-        const float *vj = v + s.L.off(s.N, sb, j, s.Hkv, kvh, D);
+        const int64_t koff = s.L.off(s.N, sb, j, s.Hkv, kvh, D);
+        if (!ULY_IN_BOUNDS(s.status, koff, D, s.kv_elems, 0x02))
+            break;
+        const float *kj = k + koff;
+        const float *vj = v + koff;
         float part = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e)
@@ -88,13 +94,14 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(AttnShape s, const
             acc[e] = fmaf(p, vj[lane + 32 * e], acc[e] * alpha);
         m = m_new;
     }
-    float *oi = o + s.L.off(s.N, sb, i, s.Hq, h, D);
+    float *oi = o + qoff;
     const float inv = 1.f / l;
 #pragma unroll
     for (int e = 0; e < E; ++e)
         oi[lane + 32 * e] = acc[e] * inv;
-    if (lane == 0)
-        lse[(sb * s.Hq + h) * s.N + i] = m + logf(l);
+    const int64_t li = (sb * s.Hq + h) * s.N + i;
+    if (lane == 0 && ULY_IN_BOUNDS(s.status, li, 1, s.lse_elems, 0x03))
+        lse[li] = m + logf(l);
 }
 
 // D_i = <dO_i, O_i>, stored [SB][Hq][N]
@@ -111,13 +118,16 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_pre_f32_kernel(AttnShape s, c
     if (i >= s.N)
         return;
     const int64_t off = s.L.off(s.N, sb, i, s.Hq, h, D);
+    const int64_t li = (sb * s.Hq + h) * s.N + i;
+    if (!ULY_IN_BOUNDS(s.status, off, D, s.q_elems, 0x04) || !ULY_IN_BOUNDS(s.status, li, 1, s.lse_elems, 0x05))
+        return;
     float part = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e)
         part = fmaf(dout[off + lane + 32 * e], o[off + lane + 32 * e], part);
     part = warp_sum(part);
     if (lane == 0)
-        Dv[(sb * s.Hq + h) * s.N + i] = part;
+        Dv[li] = part;
 }
 
 template <int D>
@@ -138,6 +148,9 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_f32_kernel(AttnShape s, co
         return;
     const int kvh = h / (s.Hq / s.Hkv);
     const int64_t off = s.L.off(s.N, sb, i, s.Hq, h, D);
+    if (!ULY_IN_BOUNDS(s.status, off, D, s.q_elems, 0x06) ||
+        !ULY_IN_BOUNDS(s.status, (sb * s.Hq + h) * s.N + i, 1, s.lse_elems, 0x07))
+        return;
     float qr[E], dor[E], acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -152,8 +165,11 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_f32_kernel(AttnShape s, co
     if (s.causal)
         hi = i + 1;
     for (int64_t j = lo; j < hi; ++j) {
-        const float *kj = k + s.L.off(s.N, sb, j, s.Hkv, kvh, D);
-        const float *vj = v + s.L.off(s.N, sb, j, s.Hkv, kvh, D);
+        const int64_t koff = s.L.off(s.N, sb, j, s.Hkv, kvh, D);
+        if (!ULY_IN_BOUNDS(s.status, koff, D, s.kv_elems, 0x08))
+            break;
+        const float *kj = k + koff;
+        const float *vj = v + koff;
         float ps = 0.f, pd = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
@@ -189,6 +205,8 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkv_f32_kernel(AttnShape s, c
         return;
     const int G = s.Hq / s.Hkv;
     const int64_t off = s.L.off(s.N, sb, j, s.Hkv, kvh, D);
+    if (!ULY_IN_BOUNDS(s.status, off, D, s.kv_elems, 0x09))
+        return;
     float kr[E], vr[E], ak[E], av[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -204,6 +222,9 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkv_f32_kernel(AttnShape s, c
     for (int h = kvh * G; h < (kvh + 1) * G; ++h) {
         for (int64_t i = lo; i < hi; ++i) {
             const int64_t qo = s.L.off(s.N, sb, i, s.Hq, h, D);
+            if (!ULY_IN_BOUNDS(s.status, qo, D, s.q_elems, 0x0a) ||
+                !ULY_IN_BOUNDS(s.status, (sb * s.Hq + h) * s.N + i, 1, s.lse_elems, 0x0b))
+                break;
             float ps = 0.f, pd = 0.f;
 #pragma unroll
             for (int e = 0; e < E; ++e) {

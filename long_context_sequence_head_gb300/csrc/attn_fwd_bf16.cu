@@ -54,6 +54,7 @@ struct FwdParams {
     float scale_log2;
     uint16_t *o;
     float *lse;
+    int64_t o_elems, lse_elems;  // extents for the bounds checks of debug builds
     WaitCfg w;
     RowLayout L;
 };
@@ -443,12 +444,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                      __uint_as_float(o32[2 * c + 1]) * inv);
                 }
                 if (row < p.N) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + p.L.off(p.N, sb, row, p.Hq, h, kD));
+                    const int64_t ooff = p.L.off(p.N, sb, row, p.Hq, h, kD);
+                    const int64_t li = (static_cast<int64_t>(sb) * p.Hq + h) * p.N + row;
+                    if (ULY_IN_BOUNDS(p.w.status, ooff, kD, p.o_elems, 0x11)) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.o + ooff);
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
-                    p.lse[(static_cast<int64_t>(sb) * p.Hq + h) * p.N + row] =
-                        (m + __log2f(l)) * 0.69314718055994530942f;
+                        for (int c = 0; c < 16; ++c)
+                            dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+                    }
+                    if (ULY_IN_BOUNDS(p.w.status, li, 1, p.lse_elems, 0x12))
+                        p.lse[li] = (m + __log2f(l)) * 0.69314718055994530942f;
                 }
             }
         }
@@ -505,6 +510,8 @@ cudaError_t launch_attn_fwd_bf16(const AttnShape &s, const void *q, const void *
     p.scale_log2 = s.scale * 1.4426950408889634f;
     p.o = static_cast<uint16_t *>(o);
     p.lse = lse;
+    p.o_elems = s.q_elems;
+    p.lse_elems = s.lse_elems;
     p.w = wait_cfg();
     p.L = s.L;
     const int64_t units = p.SB * p.Hkv * p.npairs * p.n_qtiles;

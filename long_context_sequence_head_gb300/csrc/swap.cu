@@ -52,6 +52,7 @@ struct SwapTensor {
     int64_t nchunks;     // ceil(Np / T)
     int64_t item0;       // first item of this tensor in the batch's list
     int64_t nitems;      // P (src shard) * B * nchunks * P (dst head block)
+    int64_t head_bytes;  // extent of the head-layout buffer (bounds checks of debug builds)
     int T;               // tokens per work item (TMA box height)
     int to_head;         // 1: seq->head, 0: head->seq
 };
@@ -136,8 +137,10 @@ __global__ void __launch_bounds__(32, 1) swap_kernel(const __grid_constant__ Swa
                         x.s * static_cast<int>(p.B) + x.b);
         } else {
             const uint32_t bytes = static_cast<uint32_t>(x.nt * t.row_bytes);
-            mbar_expect_tx(&full[st], bytes);
-            bulk_g2s(buf, head_ptr(p, x), bytes, &full[st]);
+            const bool ok = ULY_IN_BOUNDS(p.w.status, head_ptr(p, x) - t.head, bytes, t.head_bytes, 0x31);
+            mbar_expect_tx(&full[st], ok ? bytes : 0u);
+            if (ok)
+                bulk_g2s(buf, head_ptr(p, x), bytes, &full[st]);
         }
     };
 
@@ -157,7 +160,8 @@ __global__ void __launch_bounds__(32, 1) swap_kernel(const __grid_constant__ Swa
         }
         const uint8_t *buf = smem + static_cast<int64_t>(st) * p.stage_alloc;
         if (t.to_head) {
-            bulk_s2g(head_ptr(p, x), buf, static_cast<uint32_t>(x.nt * t.row_bytes));
+            if (ULY_IN_BOUNDS(p.w.status, head_ptr(p, x) - t.head, x.nt * t.row_bytes, t.head_bytes, 0x32))
+                bulk_s2g(head_ptr(p, x), buf, static_cast<uint32_t>(x.nt * t.row_bytes));
         } else {
             // strided seq-side scatter; tokens past Np are clipped by the map
             fence_async_smem();
@@ -250,6 +254,7 @@ cudaError_t launch_swap_batch(const SwapDesc *descs, int n, int64_t B, int64_t N
         t.nchunks = (Np + T - 1) / T;
         t.item0 = items;
         t.nitems = static_cast<int64_t>(P) * B * t.nchunks * P;
+        t.head_bytes = B * N * static_cast<int64_t>(H) * d * esize;
         t.to_head = to_head ? 1 : 0;
         items += t.nitems;
     }

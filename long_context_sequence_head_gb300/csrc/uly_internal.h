@@ -118,6 +118,11 @@ struct AttnShape {
     int num_docs;
     float scale;      // softmax scale
     RowLayout L;     // where q/k/v/o/dout/dq/dk/dv rows live
+    // buffer extents in elements, for the bounds checks of debug builds
+    int64_t q_elems;    // q, o, dout, dq
+    int64_t kv_elems;   // k, v, dk, dv
+    int64_t lse_elems;  // lse (and the per-row fp32 scratch)
+    unsigned *status;   // device status word
 };
 
 // 5-D bf16 tensor map {d, H, T, B, outer} over a row-major

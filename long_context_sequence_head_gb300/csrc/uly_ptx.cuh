@@ -11,13 +11,36 @@
 namespace uly {
 
 // ---------------------------------------------------------------- status
-// Device status word (see ulysses_get_device_status).  Bit 0: a bounded wait
-// ran out; bits 8..15: the id of the first site that ran out; bit 1: a kernel
-// found an argument it could not handle.
+// Device status word (see ulysses_get_device_status).  Word 0 holds flags:
+// bit 0, a bounded wait ran out; bit 1, a kernel found an argument it could
+// not handle; bit 2, a bounds check of a debug build failed.  Word 1 holds
+// the id of the first site that reported.
 enum : unsigned {
     kDevTimeout = 1u << 0,
     kDevBadArg = 1u << 1,
+    kDevBounds = 1u << 2,
 };
+
+// Debug builds (-DULY_DEBUG) check every raw-pointer global access of the
+// hot-path kernels against its buffer: the elements [off, off + n) must lie in
+// [0, extent).  A failed check sets kDevBounds, records the site (0x8000 plus
+// a per-access id) and tells the caller to skip the access, so an indexing
+// mistake becomes a status the host reads instead of a stray write.  Release
+// builds compile every check to `true`.  (TMA copies need no check: the
+// tensor map clips them to the tensor's extent.)
+#ifdef ULY_DEBUG
+__device__ __forceinline__ bool bounds_ok(unsigned *status, int64_t off, int64_t n, int64_t extent, unsigned id)
+{
+    if (off >= 0 && n >= 0 && off + n <= extent)
+        return true;
+    atomicOr(status, kDevBounds);
+    atomicCAS(status + 1, 0u, 0x8000u | id);
+    return false;
+}
+#define ULY_IN_BOUNDS(status, off, n, extent, id) ::uly::bounds_ok((status), (off), (n), (extent), (id))
+#else
+#define ULY_IN_BOUNDS(status, off, n, extent, id) true
+#endif
 
 struct WaitCfg {
     unsigned *status;     // device status word

@@ -43,6 +43,14 @@ int current_device()
     return dev;
 }
 
+__global__ void selftest_bounds_kernel(unsigned *status)
+{
+    // an access of 4 elements at offset 8 of a 4-element buffer: the check
+    // fails and reports; nothing is read or written
+    if (threadIdx.x == 0 && ULY_IN_BOUNDS(status, 8, 4, 4, 0x7f))
+        atomicOr(status, uly::kDevBadArg);  // reached only if the check passed
+}
+
 __global__ void selftest_timeout_kernel(uly::WaitCfg w)
 {
     __shared__ __align__(8) uint64_t bar;
@@ -311,6 +319,10 @@ uly_status attn_fwd_impl(const void *q, const void *k, const void *v, void *o, f
     sh.cu_host = cu_seqlens_host;
     sh.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
     sh.L = L;
+    sh.q_elems = sh.SB * N * Hq_local * d;
+    sh.kv_elems = sh.SB * N * Hkv_local * d;
+    sh.lse_elems = sh.SB * N * Hq_local;
+    sh.status = uly::device_status_ptr();
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     if (cu_seqlens_host) {
         int32_t *cu_dev = reinterpret_cast<int32_t *>(ws + W.cu_off);
@@ -359,6 +371,10 @@ uly_status attn_bwd_impl(const void *q, const void *k, const void *v, const void
     sh.cu_host = cu_seqlens_host;
     sh.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
     sh.L = L;
+    sh.q_elems = sh.SB * N * Hq_local * d;
+    sh.kv_elems = sh.SB * N * Hkv_local * d;
+    sh.lse_elems = sh.SB * N * Hq_local;
+    sh.status = uly::device_status_ptr();
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     if (cu_seqlens_host) {
         int32_t *cu_dev = reinterpret_cast<int32_t *>(ws + W.cu_off);
@@ -563,6 +579,8 @@ uly_status ulysses_get_device_status(void *stream, uint32_t *site_out)
         *site_out = host[1];
     if (host[0] & uly::kDevTimeout)
         return ULY_ERR_TIMEOUT;
+    if (host[0] & uly::kDevBounds)
+        return ULY_ERR_BOUNDS;
     if (host[0] & uly::kDevBadArg)
         return ULY_ERR_INVALID_ARG;
     return ULY_OK;
@@ -581,6 +599,20 @@ uly_status ulysses_selftest_wait_timeout(uint64_t limit_ns, void *stream)
     if (limit_ns < 1000 || limit_ns > 10000000000ull)
         return ULY_ERR_INVALID_ARG;
     return from_cuda(uly::launch_selftest_timeout(limit_ns, static_cast<cudaStream_t>(stream)));
+}
+
+uly_status ulysses_selftest_bounds(void *stream)
+{
+#ifdef ULY_DEBUG
+    unsigned *status = uly::device_status_ptr();
+    if (status == nullptr)
+        return ULY_ERR_CUDA;
+    selftest_bounds_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
+    return from_cuda(cudaGetLastError());
+#else
+    (void)stream;
+    return ULY_ERR_UNSUPPORTED;
+#endif
 }
 
 const char *ulysses_status_string(uly_status status)
@@ -604,6 +636,8 @@ const char *ulysses_status_string(uly_status status)
         return "workspace missing or too small";
     case ULY_ERR_SCRATCH_LIMIT:
         return "sizes exceed the fixed scratch of the no-allocation entry point";
+    case ULY_ERR_BOUNDS:
+        return "a bounds check of the debug build failed";
     }
     return "unknown status";
 }

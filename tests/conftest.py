@@ -26,7 +26,7 @@ def uly():
     """The CUDA library binding, built in-tree if needed."""
     import long_context_sequence_head_gb300 as m
     from long_context_sequence_head_gb300 import build as b
-    b.build()
+    b.build(debug=m.debug_build_selected())
     m.load()
     # tests bound every device-side wait to 250 ms so a broken pipeline fails fast
     m.ulysses_set_wait_limit_ns(250_000_000)

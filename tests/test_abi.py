@@ -30,9 +30,24 @@ def test_exports_every_declared_symbol(uly):
 
 def test_version_and_strings(uly):
     assert uly.ulysses_version() == 100
-    for code in range(9):
+    for code in range(10):
         assert uly.ulysses_status_string(code)
     assert uly.ulysses_status_string(0) == "ok"
+
+
+def test_release_build_has_no_bounds_selftest(uly):
+    """The bounds checks exist only in the debug build; the release library
+    answers its self-test with ULY_ERR_UNSUPPORTED and launches nothing."""
+    if uly.debug_build_selected():
+        pytest.skip("this process runs the debug build")
+    assert uly.load().ulysses_selftest_bounds(None) == UNSUPPORTED
+
+
+def test_debug_build_exports_every_declared_symbol(uly):
+    from long_context_sequence_head_gb300 import build as b
+    lib = ctypes.CDLL(b.build(debug=True))
+    for n in _declared():
+        assert hasattr(lib, n), n
 
 
 def _swap(lib, a, b, B, N, H, d, P, dt=BF16):
