@@ -293,6 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_fence32p(u + cb);
                 const int64_t key0 = static_cast<int64_t>(kt_lo + j) * kBN;
                 const bool masked = key0 < lo || key0 + kBN > hi;
+                // no key of this tile is allowed for this row (a row of a later
+                // document in a query tile that straddles a document boundary)
+                const bool row_empty = key0 >= hi || key0 + kBN <= lo;
                 if (masked) {
                     // allowed columns of this tile: [lo_c, hi_c)
                     const int lo_c = static_cast<int>(max(lo - key0, int64_t(0)));
@@ -305,17 +308,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Speculate that the running maximum m still holds: the tile's
                 // exponentials against m all stay <= 2^8 exactly when the lazy
                 // rescale rule would keep m, and their sum <= 2^8 proves it.  On
-                // a row's first tile, or when the sum says the maximum may have
-                // grown, the tile is redone exactly from S, still in TMEM.
+                // a row's first tile with an allowed key, or when the sum says the
+                // maximum may have grown, the tile is redone exactly from S, still
+                // in TMEM.  A row that has seen no allowed key yet and has none in
+                // this tile either takes the speculative pass against 0: all its
+                // scores are -inf, its exponentials exactly 0.
                 const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
                 float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
-                const bool first = __any_sync(0xffffffffu, m == -INFINITY);
+                const bool first = __any_sync(0xffffffffu, m == -INFINITY && !row_empty);
                 if (!first) {
                     // p = 2^(s * scale * log2(e) - m) on the SFU (masked scores are
                     // -inf and give exactly 0); the scale-and-shift and the row sum
                     // run as packed f32x2 pairs, the sum in four independent chains
-                    const float2 nm2 = make_float2(-m, -m);
+                    const float m_ref = (m == -INFINITY) ? 0.f : m;
+                    const float2 nm2 = make_float2(-m_ref, -m_ref);
 #pragma unroll
                     for (int c = 0; c < kBN; c += 2) {
                         const float2 x = ffma2(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2, nm2);
