@@ -242,10 +242,22 @@ def ulysses_swap_batch(items, P: int, stream=None):
 
 # ------------------------------------------------ all-to-all across GPUs
 
-def _a2a_shapes(x, P, what):
+def _a2a_shapes(x, what):
     if x.dim() != 4 or x.shape[0] != 1:
         raise ValueError(f"{what} must be [1][tokens][heads][d] (batch 1), got {tuple(x.shape)}")
+    if not x.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
     return x.shape[1], x.shape[2], x.shape[3]
+
+
+def _a2a_out(out, shape, like, what):
+    """A caller-supplied output buffer, checked, or a new one."""
+    if out is None:
+        return torch.empty(*shape, dtype=like.dtype, device=like.device)
+    if (tuple(out.shape) != tuple(shape) or out.dtype != like.dtype or out.device != like.device
+            or not out.is_contiguous()):
+        raise ValueError(f"{what} must be a contiguous {tuple(shape)} tensor of {like.dtype} on {like.device}")
+    return out
 
 
 def ulysses_a2a_pack(x_local: torch.Tensor, P: int, out: Optional[torch.Tensor] = None, stream=None):
@@ -254,11 +266,10 @@ def ulysses_a2a_pack(x_local: torch.Tensor, P: int, out: Optional[torch.Tensor] 
     contiguous blocks [P][1][T][H/P][d], block s holding head block s for
     rank s.  It is the library's seq->head kernel applied to the rank's own
     shard seen as P sub-shards of T/P tokens (so T % P == 0)."""
-    T, H, d = _a2a_shapes(x_local, P, "x_local")
+    T, H, d = _a2a_shapes(x_local, "x_local")
     if T % P or H % P:
         raise ValueError(f"the local tokens ({T}) and the heads ({H}) must be multiples of P={P}")
-    if out is None:
-        out = torch.empty(P, 1, T, H // P, d, dtype=x_local.dtype, device=x_local.device)
+    out = _a2a_out(out, (P, 1, T, H // P, d), x_local, "out")
     ulysses_seq_to_head(x_local.view(P, 1, T // P, H, d), out, P, stream)
     return out
 
@@ -268,11 +279,12 @@ def ulysses_a2a_unpack(recv: torch.Tensor, P: int, out: Optional[torch.Tensor] =
     (block s = head block s of this rank's T tokens, from rank s) back to the
     sequence shard [1][T][H][d]: the library's head->seq kernel on the rank's
     own tokens."""
+    if recv.dim() != 5 or not recv.is_contiguous():
+        raise ValueError(f"recv must be a contiguous [P={P}][1][T][H/P][d] tensor, got {tuple(recv.shape)}")
     Ps, B, T, Hp, d = recv.shape
     if Ps != P or B != 1 or T % P:
         raise ValueError(f"recv must be [P={P}][1][T][H/P][d] with T % P == 0, got {tuple(recv.shape)}")
-    if out is None:
-        out = torch.empty(1, T, Hp * P, d, dtype=recv.dtype, device=recv.device)
+    out = _a2a_out(out, (1, T, Hp * P, d), recv, "out")
     ulysses_head_to_seq(recv, out.view(P, 1, T // P, Hp * P, d), P, stream)
     return out
 
@@ -292,12 +304,9 @@ def ulysses_all_to_all_seq_to_head(x_local: torch.Tensor, group=None, out: Optio
     copy.  Per rank (P-1)/P of the shard crosses the network: O(N d / P)."""
     import torch.distributed as dist
     P = dist.get_world_size(group)
-    T, H, d = _a2a_shapes(x_local, P, "x_local")
+    T, H, d = _a2a_shapes(x_local, "x_local")
     send = ulysses_a2a_pack(x_local, P)
-    if out is None:
-        out = torch.empty(1, P * T, H // P, d, dtype=x_local.dtype, device=x_local.device)
-    if tuple(out.shape) != (1, P * T, H // P, d) or not out.is_contiguous():
-        raise ValueError(f"out must be a contiguous [1][{P * T}][{H // P}][{d}] tensor")
+    out = _a2a_out(out, (1, P * T, H // P, d), x_local, "out")
     dist.all_to_all_single(out.view(P, T * (H // P) * d), send.view(P, T * (H // P) * d), group=group)
     return out
 
@@ -311,12 +320,12 @@ def ulysses_all_to_all_head_to_seq(x_head: torch.Tensor, group=None, out: Option
     the sequence layout by the library's head->seq kernel."""
     import torch.distributed as dist
     P = dist.get_world_size(group)
-    N, Hp, d = _a2a_shapes(x_head, P, "x_head")
+    N, Hp, d = _a2a_shapes(x_head, "x_head")
     if N % P:
         raise ValueError(f"the tokens ({N}) must be a multiple of P={P}")
     T = N // P
     recv = torch.empty(P, 1, T, Hp, d, dtype=x_head.dtype, device=x_head.device)
-    dist.all_to_all_single(recv.view(P, T * Hp * d), x_head.contiguous().view(P, T * Hp * d), group=group)
+    dist.all_to_all_single(recv.view(P, T * Hp * d), x_head.view(P, T * Hp * d), group=group)
     return ulysses_a2a_unpack(recv, P, out)
 
 

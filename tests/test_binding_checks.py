@@ -81,3 +81,20 @@ def test_sharded_loss_arguments():
         uly.ulysses_sharded_ce_loss(logits, labels, P, dlogits=_t(P, B, Np, V, dtype=torch.float32))
     with pytest.raises(ValueError, match="logits must be"):
         uly.ulysses_sharded_ce_loss(logits, labels, 4)
+
+
+def test_all_to_all_helpers_check_their_buffers():
+    """The exchange's pack/unpack refuse non-contiguous inputs and outputs of
+    the wrong shape, dtype or device before any kernel is reached."""
+    import long_context_sequence_head_gb300 as uly
+    x = torch.zeros(1, 8, 4, 64)
+    with pytest.raises(ValueError):
+        uly.ulysses_a2a_pack(x.transpose(1, 2), 2)                      # not contiguous
+    with pytest.raises(ValueError):
+        uly.ulysses_a2a_pack(torch.zeros(2, 8, 4, 64), 2)               # batch 2
+    with pytest.raises(ValueError):
+        uly.ulysses_a2a_pack(x, 2, out=torch.zeros(2, 1, 8, 2, 32))     # wrong out shape
+    with pytest.raises(ValueError):
+        uly.ulysses_a2a_pack(x, 2, out=torch.zeros(2, 1, 8, 2, 64, dtype=torch.float64))
+    with pytest.raises(ValueError):
+        uly.ulysses_a2a_unpack(torch.zeros(2, 1, 7, 2, 64), 2)          # T not a multiple of P
