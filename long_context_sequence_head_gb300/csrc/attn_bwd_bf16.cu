@@ -62,6 +62,7 @@ struct BwdParams {
     int64_t SB, N, Npad;
     int Hq, Hkv, G, n_ktiles;
     int group;  // problems interleaved in the grid
+    const int32_t *order;  // with documents: key tiles, longest walk first
     int causal;
     const int32_t *cu;
     int num_docs;
@@ -225,7 +226,9 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
 }
 
 // ----------------------------------------------------------------- main
-template <bool kGrouped>
+// kDecode: 0 = problem-major, key tiles in index order; 1 = groups of
+// problems interleaved; 2 = the same with the host's key-tile order.
+template <int kDecode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -266,9 +269,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile's walk is long next to a problem's share of the GPU (short
     // sequences, documents), the last problem's longest walks would run on
     // alone at the end; there groups of problems interleave their key tiles
-    // instead (the launcher picks the group size) ----
+    // instead (the launcher picks the group size).  With documents a key
+    // tile's walk follows its place in its document, and the host's order
+    // puts the longest walks first ----
     int n_blk, prob;
-    if constexpr (!kGrouped) {
+    if constexpr (kDecode == 0) {
         n_blk = static_cast<int>(blockIdx.x % p.n_ktiles);
         prob = static_cast<int>(blockIdx.x / p.n_ktiles);
     } else {
@@ -277,7 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t grp = blockIdx.x / (static_cast<int64_t>(p.group) * p.n_ktiles);
         const int64_t rem = blockIdx.x % (static_cast<int64_t>(p.group) * p.n_ktiles);
         const int64_t gsize = (nprob - grp * p.group < p.group) ? nprob - grp * p.group : p.group;
-        n_blk = static_cast<int>(rem / gsize);
+        const int rank = static_cast<int>(rem / gsize);
+        n_blk = kDecode == 2 ? p.order[rank] : rank;
         prob = static_cast<int>(grp * p.group + rem % gsize);
     }
     const int kvh = prob % p.Hkv;
@@ -714,7 +720,8 @@ cudaError_t launch_attn_bwd_bf16(const AttnShape &s, const void *q, const void *
         p.group = group_for(work, longest, s.SB * s.Hkv);
     }
     const size_t smem = BwdSmem::kTotal;
-    auto kernel = p.group > 1 ? attn_bwd_bf16_kernel<true> : attn_bwd_bf16_kernel<false>;
+    p.order = s.order_dev;
+    auto kernel = p.order ? attn_bwd_bf16_kernel<2> : p.group > 1 ? attn_bwd_bf16_kernel<1> : attn_bwd_bf16_kernel<0>;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess)

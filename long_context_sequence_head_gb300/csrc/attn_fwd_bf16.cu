@@ -55,6 +55,7 @@ struct FwdParams {
     uint16_t *o;
     float *lse;
     int64_t o_elems, lse_elems;  // extents for the bounds checks of debug builds
+    const int32_t *order;        // with documents: query tiles, longest walk first
     WaitCfg w;
     RowLayout L;
 };
@@ -77,6 +78,7 @@ __device__ __forceinline__ void doc_range(const FwdParams &p, int64_t i, int64_t
     hi = p.cu[a + 1];
 }
 
+template <bool kOrdered>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, FwdParams p)
@@ -99,10 +101,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- work unit: problem-major (resident CTAs share one (shard*batch,
     // KV head) problem and stream the same K/V tiles through L2), longest
-    // query blocks first within a problem ----
+    // query blocks first within a problem: the last blocks without documents,
+    // the host's order with them ----
     const int64_t u = blockIdx.x;
     const int pair = static_cast<int>(u % p.npairs);
-    const int m_blk = p.n_qtiles - 1 - static_cast<int>((u / p.npairs) % p.n_qtiles);
+    const int rank = static_cast<int>((u / p.npairs) % p.n_qtiles);
+    const int m_blk = kOrdered ? p.order[rank] : p.n_qtiles - 1 - rank;
     const int64_t prob = u / (static_cast<int64_t>(p.npairs) * p.n_qtiles);
     const int kvh = static_cast<int>(prob % p.Hkv);
     const int sb = static_cast<int>(prob / p.Hkv);
@@ -521,13 +525,14 @@ cudaError_t launch_attn_fwd_bf16(const AttnShape &s, const void *q, const void *
     p.lse_elems = s.lse_elems;
     p.w = wait_cfg();
     p.L = s.L;
+    p.order = s.order_dev;
     const int64_t units = p.SB * p.Hkv * p.npairs * p.n_qtiles;
     const size_t smem = FwdSmem::kTotal + 1024;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    auto kernel = p.order ? attn_fwd_bf16_kernel<true> : attn_fwd_bf16_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    attn_fwd_bf16_kernel<<<static_cast<unsigned>(units), kThreads, smem, stream>>>(tq, tk, tv, p);
+    kernel<<<static_cast<unsigned>(units), kThreads, smem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 

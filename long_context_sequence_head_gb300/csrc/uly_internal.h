@@ -6,6 +6,9 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "uly_ptx.cuh"
 
 namespace uly {
@@ -35,6 +38,30 @@ inline void doc_range_host(const int32_t *cu, int num_docs, int64_t N, int64_t i
     }
     lo = cu[a];
     hi = cu[a + 1];
+}
+
+// The 128-row tiles of a packed-document sequence in the order the bf16
+// kernels walk them, longest walk first, so that no long walk is left to run
+// on alone at the end of a launch (with documents the walk length follows a
+// tile's place in its document, not its index).  Forward (bwd = false): query
+// tiles, walk = the key tiles their rows may attend to, ties with the later
+// tile first.  Backward: key tiles, walk = the query tiles that may attend to
+// them, ties with the earlier tile first.  out: ceil(N/128) entries.
+inline void tile_order_host(bool bwd, int64_t N, int causal, const int32_t *cu, int num_docs, int32_t *out)
+{
+    const int n = static_cast<int>((N + 127) / 128);
+    std::vector<int64_t> walk(n);
+    for (int t = 0; t < n; ++t) {
+        const int64_t a = static_cast<int64_t>(t) * 128, b = std::min<int64_t>(a + 127, N - 1);
+        int64_t lo_a, hi_a, lo_b, hi_b;
+        doc_range_host(cu, num_docs, N, a, lo_a, hi_a);
+        doc_range_host(cu, num_docs, N, b, lo_b, hi_b);
+        const int64_t lo = (bwd && causal) ? a : lo_a;
+        const int64_t hi = (!bwd && causal) ? b + 1 : hi_b;
+        walk[t] = (hi - 1) / 128 - lo / 128 + 1;
+        out[t] = bwd ? t : n - 1 - t;
+    }
+    std::stable_sort(out, out + n, [&](int32_t x, int32_t y) { return walk[x] > walk[y]; });
 }
 
 // Problems interleaved per group of the grid: the fewest that make a group's
@@ -115,6 +142,7 @@ struct AttnShape {
     int causal;
     const int32_t *cu_dev;  // device cu_seqlens [num_docs+1] or nullptr
     const int32_t *cu_host; // the same on the host (valid during the call) or nullptr
+    int32_t *order_dev;     // with documents: device room for a 128-row tile order [ceil(N/128)], else nullptr
     int num_docs;
     float scale;      // softmax scale
     RowLayout L;     // where q/k/v/o/dout/dq/dk/dv rows live

@@ -65,10 +65,12 @@ __global__ void selftest_timeout_kernel(uly::WaitCfg w)
 // Workspace layout (every region 256-byte aligned):
 //   [0, 256)          reserved
 //   cu_seqlens copy   (num_docs + 1) int32, if documents are packed
+//   tile order        ceil(N/128) int32, if documents are packed (the bf16
+//                     kernels' walk order, longest walks first)
 //   bf16 backward     lse2 [SB][Hq][Npad], D [SB][Hq][Npad], dq_acc [SB][Hq][Npad][d]
 //   fp32 backward     D [SB][Hq][N]
 struct WsLayout {
-    size_t cu_off = 0, lse2_off = 0, D_off = 0, acc_off = 0, total = 0;
+    size_t cu_off = 0, order_off = 0, lse2_off = 0, D_off = 0, acc_off = 0, total = 0;
     int64_t Npad = 0;
 };
 
@@ -79,6 +81,9 @@ WsLayout ws_layout(int64_t B, int64_t N, int Hq, int d, int S, int num_docs, boo
     L.cu_off = off;
     if (num_docs > 0)
         off += align_up(static_cast<size_t>(num_docs + 1) * sizeof(int32_t));
+    L.order_off = off;
+    if (num_docs > 0)
+        off += align_up(static_cast<size_t>((N + 127) / 128) * sizeof(int32_t));
     const int64_t SB = static_cast<int64_t>(S) * B;
     L.Npad = (N + 127) / 128 * 128;
     if (bwd) {
@@ -317,6 +322,7 @@ uly_status attn_fwd_impl(const void *q, const void *k, const void *v, void *o, f
     sh.num_docs = cu_seqlens_host ? num_docs : 0;
     sh.cu_dev = nullptr;
     sh.cu_host = cu_seqlens_host;
+    sh.order_dev = nullptr;
     sh.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
     sh.L = L;
     sh.q_elems = sh.SB * N * Hq_local * d;
@@ -325,12 +331,18 @@ uly_status attn_fwd_impl(const void *q, const void *k, const void *v, void *o, f
     sh.status = uly::device_status_ptr();
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     if (cu_seqlens_host) {
-        int32_t *cu_dev = reinterpret_cast<int32_t *>(ws + W.cu_off);
-        cudaError_t e = cudaMemcpyAsync(cu_dev, cu_seqlens_host, sizeof(int32_t) * (num_docs + 1),
+        // cu_seqlens and the tile walk order, adjacent in the workspace: one
+        // copy (from pageable memory, staged before the call returns)
+        std::vector<int32_t> host((W.order_off - W.cu_off) / sizeof(int32_t) + (N + 127) / 128);
+        std::copy(cu_seqlens_host, cu_seqlens_host + num_docs + 1, host.begin());
+        uly::tile_order_host(false, N, causal, cu_seqlens_host, num_docs,
+                             host.data() + (W.order_off - W.cu_off) / sizeof(int32_t));
+        cudaError_t e = cudaMemcpyAsync(ws + W.cu_off, host.data(), host.size() * sizeof(int32_t),
                                         cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess)
             return ULY_ERR_CUDA;
-        sh.cu_dev = cu_dev;
+        sh.cu_dev = reinterpret_cast<int32_t *>(ws + W.cu_off);
+        sh.order_dev = reinterpret_cast<int32_t *>(ws + W.order_off);
     }
     if (dtype == ULY_FP32)
         return from_cuda(uly::launch_attn_fwd_f32(sh, static_cast<const float *>(q), static_cast<const float *>(k),
@@ -369,6 +381,7 @@ uly_status attn_bwd_impl(const void *q, const void *k, const void *v, const void
     sh.num_docs = cu_seqlens_host ? num_docs : 0;
     sh.cu_dev = nullptr;
     sh.cu_host = cu_seqlens_host;
+    sh.order_dev = nullptr;
     sh.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
     sh.L = L;
     sh.q_elems = sh.SB * N * Hq_local * d;
@@ -377,12 +390,18 @@ uly_status attn_bwd_impl(const void *q, const void *k, const void *v, const void
     sh.status = uly::device_status_ptr();
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     if (cu_seqlens_host) {
-        int32_t *cu_dev = reinterpret_cast<int32_t *>(ws + W.cu_off);
-        cudaError_t e = cudaMemcpyAsync(cu_dev, cu_seqlens_host, sizeof(int32_t) * (num_docs + 1),
+        // cu_seqlens and the tile walk order, adjacent in the workspace: one
+        // copy (from pageable memory, staged before the call returns)
+        std::vector<int32_t> host((W.order_off - W.cu_off) / sizeof(int32_t) + (N + 127) / 128);
+        std::copy(cu_seqlens_host, cu_seqlens_host + num_docs + 1, host.begin());
+        uly::tile_order_host(true, N, causal, cu_seqlens_host, num_docs,
+                             host.data() + (W.order_off - W.cu_off) / sizeof(int32_t));
+        cudaError_t e = cudaMemcpyAsync(ws + W.cu_off, host.data(), host.size() * sizeof(int32_t),
                                         cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess)
             return ULY_ERR_CUDA;
-        sh.cu_dev = cu_dev;
+        sh.cu_dev = reinterpret_cast<int32_t *>(ws + W.cu_off);
+        sh.order_dev = reinterpret_cast<int32_t *>(ws + W.order_off);
     }
     if (dtype == ULY_FP32)
         return from_cuda(uly::launch_attn_bwd_f32(
