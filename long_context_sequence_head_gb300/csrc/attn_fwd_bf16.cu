@@ -52,9 +52,8 @@ struct FwdParams {
     const int32_t *cu;
     int num_docs;
     float scale_log2;
-    uint16_t *o;
     float *lse;
-    int64_t o_elems, lse_elems;  // extents for the bounds checks of debug builds
+    int64_t lse_elems;  // extent for the bounds checks of debug builds
     const int32_t *order;        // with documents: query tiles, longest walk first
     WaitCfg w;
     RowLayout L;
@@ -81,7 +80,8 @@ __device__ __forceinline__ void doc_range(const FwdParams &p, int64_t i, int64_t
 template <bool kOrdered>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, FwdParams p)
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                         FwdParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_o);
             mbar_expect_tx(q_full, has1 ? 2 * kTileBytes : kTileBytes);
             int c1, c2, c3, c4;
             p.L.tile(sb, q0, p.Hq, h0, c1, c2, c3, c4);
@@ -439,10 +440,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok)
                 *abort_flag = 1;
-            if (mbar_wait_warp(o_done, 0, p.w, 0x48 + t) && ok) {
+            // O epilogue: row r, normalised to bf16, into this head's Q tile
+            // (free once o_done has seen every product complete) in the
+            // 128-byte swizzled layout of the tensor map, then one thread
+            // stores the 128-row tile with two TMA copies (rows past the end
+            // are clipped by the map).  One thread per row writing its own
+            // 256 bytes would send 32 rows through every warp-wide store.
+            const bool have_o = mbar_wait_warp(o_done, 0, p.w, 0x48 + t) && ok;
+            uint8_t *stage = smem + (t ? FwdSmem::kQ1 : FwdSmem::kQ0);
+            if (have_o) {
                 tc_fence_after();
-                float inv = 1.f / l;
-                uint32_t ob[64];
+                const float inv = 1.f / l;
 #pragma unroll
                 for (int cb = 0; cb < kD; cb += 32) {
                     uint32_t o32[32];
@@ -450,22 +458,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
                     tmem_ld_fence32p(o32);
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        ob[cb / 2 + c] = pack_bf16x2(__uint_as_float(o32[2 * c]) * inv,
-                                                     __uint_as_float(o32[2 * c + 1]) * inv);
-                }
-                if (row < p.N) {
-                    const int64_t ooff = p.L.off(p.N, sb, row, p.Hq, h, kD);
-                    const int64_t li = (static_cast<int64_t>(sb) * p.Hq + h) * p.N + row;
-                    if (ULY_IN_BOUNDS(p.w.status, ooff, kD, p.o_elems, 0x11)) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.o + ooff);
-#pragma unroll
-                        for (int c = 0; c < 16; ++c)
-                            dst[c] = make_uint4(ob[4 * c], ob[4 * c + 1], ob[4 * c + 2], ob[4 * c + 3]);
+                    for (int q = 0; q < 4; ++q) {
+                        const int unit = cb / 8 + q;  // 16-byte unit of the row, 0..15
+                        const uint4 val = make_uint4(
+                            pack_bf16x2(__uint_as_float(o32[8 * q]) * inv, __uint_as_float(o32[8 * q + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(o32[8 * q + 2]) * inv, __uint_as_float(o32[8 * q + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(o32[8 * q + 4]) * inv, __uint_as_float(o32[8 * q + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(o32[8 * q + 6]) * inv, __uint_as_float(o32[8 * q + 7]) * inv));
+                        *reinterpret_cast<uint4 *>(stage + (unit >> 3) * kChunk + r * 128 +
+                                                   (((unit & 7) ^ (r & 7)) << 4)) = val;
                     }
+                }
+                fence_async_smem();
+                if (row < p.N) {
+                    const int64_t li = (static_cast<int64_t>(sb) * p.Hq + h) * p.N + row;
                     if (ULY_IN_BOUNDS(p.w.status, li, 1, p.lse_elems, 0x12))
                         p.lse[li] = (m + __log2f(l)) * 0.69314718055994530942f;
                 }
+            }
+            named_bar_sync(1 + t, 128);  // the head's four warps have staged their rows
+            if (r == 0 && have_o) {
+                int c1, c2, c3, c4;
+                p.L.tile(sb, q0, p.Hq, h, c1, c2, c3, c4);
+                tma_store_5d(&tm_o, stage, 0, c1, c2, c3, c4);
+                tma_store_5d(&tm_o, stage + kChunk, 64, c1, c2, c3, c4);
+                bulk_commit();
+                bulk_wait_read<0>();  // the tile is read before the CTA's shared memory goes
             }
         }
     }
@@ -503,9 +521,9 @@ cudaError_t launch_attn_fwd_bf16(const AttnShape &s, const void *q, const void *
 {
     if (s.d != kD)
         return cudaErrorInvalidValue;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (make_rows_map_bf16(&tq, q, s, s.Hq) != CUDA_SUCCESS || make_rows_map_bf16(&tk, k, s, s.Hkv) != CUDA_SUCCESS ||
-        make_rows_map_bf16(&tv, v, s, s.Hkv) != CUDA_SUCCESS)
+        make_rows_map_bf16(&tv, v, s, s.Hkv) != CUDA_SUCCESS || make_rows_map_bf16(&to, o, s, s.Hq) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     FwdParams p;
     p.SB = s.SB;
@@ -519,9 +537,7 @@ cudaError_t launch_attn_fwd_bf16(const AttnShape &s, const void *q, const void *
     p.cu = s.cu_dev;
     p.num_docs = s.num_docs;
     p.scale_log2 = s.scale * 1.4426950408889634f;
-    p.o = static_cast<uint16_t *>(o);
     p.lse = lse;
-    p.o_elems = s.q_elems;
     p.lse_elems = s.lse_elems;
     p.w = wait_cfg();
     p.L = s.L;
@@ -532,7 +548,7 @@ cudaError_t launch_attn_fwd_bf16(const AttnShape &s, const void *q, const void *
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    kernel<<<static_cast<unsigned>(units), kThreads, smem, stream>>>(tq, tk, tv, p);
+    kernel<<<static_cast<unsigned>(units), kThreads, smem, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 

@@ -35,16 +35,6 @@ constexpr int kSwapSmemBytes = 196608;  // largest ring of stages per CTA
 constexpr int kSwapPairRing = 98304;     // ring when two CTAs share an SM
 constexpr int kSwapMaxStages = 8;
 
-__device__ __forceinline__ void tma_store_5d(const CUtensorMap *map, const void *smem_src, int c0, int c1, int c2,
-                                             int c3, int c4)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group"
-        " [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(map),
-        "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-        : "memory");
-}
-
 // One tensor of a batch.
 struct SwapTensor {
     uint8_t *head;       // head-layout buffer (src for head->seq, dst for seq->head)
