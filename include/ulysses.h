@@ -129,6 +129,26 @@ size_t ulysses_attn_workspace_size(int64_t B, int64_t N, int32_t Hq_local, int32
                                    int32_t for_bwd, uly_dtype dtype);
 
 /*
+ * The order in which the bf16 attention kernels walk the 128-row tiles of
+ * a sequence (host only; no device work).  out[0 .. ceil(N/128)) receives
+ * every tile index once, longest walk first.  Forward (for_bwd = 0): query
+ * tiles, a tile's walk being the key tiles its rows may attend to (their
+ * documents' keys, up to the row itself when causal); ties keep the later
+ * tile first.  Backward (for_bwd = 1): key tiles, the walk being the query
+ * tiles that may attend to the keys; ties keep the earlier tile first.
+ * With packed documents a tile's walk follows its place in its document, so
+ * the attention calls sort the tiles like this themselves (the order goes
+ * into the workspace next to cu_seqlens); without documents the walk only
+ * depends on the index and this is the kernels' index order.  Exposed for
+ * inspection and tests.
+ * out : host, ceil(N/128) int32.
+ * Errors: ULY_ERR_INVALID_ARG for out == NULL, N < 1, causal or for_bwd not
+ * 0/1, or cu_seqlens the attention calls would reject.
+ */
+uly_status ulysses_attn_tile_order(int64_t N, int32_t causal, const int32_t *cu_seqlens_host,
+                                   int32_t num_docs, int32_t for_bwd, int32_t *out);
+
+/*
  * Attention forward over `num_shards` consecutive head shards (blog summary,
  * step 4 "Local Attention": every rank attends over all N tokens for its
  * heads).  For shard s, batch b, local query head h (local KV head h / G,

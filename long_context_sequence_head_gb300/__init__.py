@@ -32,6 +32,7 @@ _STATUS = {0: "ULY_OK", 1: "ULY_ERR_INVALID_ARG", 2: "ULY_ERR_UNSUPPORTED", 3: "
 
 # every symbol include/ulysses.h declares
 EXPORTED = ("ulysses_seq_to_head", "ulysses_head_to_seq", "ulysses_swap_batch", "ulysses_attn_workspace_size",
+            "ulysses_attn_tile_order",
             "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_attn_fwd_seq", "ulysses_attn_bwd_seq",
             "ulysses_attn_bwd_noalloc", "ulysses_sharded_ce_workspace_size", "ulysses_sharded_ce_loss",
             "ulysses_ring_attn_workspace_size", "ulysses_ring_attn_fwd", "ulysses_ring_attn_bwd",
@@ -78,6 +79,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.ulysses_swap_batch.argtypes = [vp, i32, i64, i64, i32, i32, i32, vp]
     lib.ulysses_attn_workspace_size.argtypes = [i64, i64, i32, i32, i32, i32, i32, i32, i32]
     lib.ulysses_attn_workspace_size.restype = sz
+    lib.ulysses_attn_tile_order.argtypes = [i64, i32, vp, i32, i32, vp]
     lib.ulysses_attn_fwd.argtypes = [vp] * 5 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp, sz, vp]
     lib.ulysses_attn_bwd.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, i32, vp, sz, vp]
     lib.ulysses_attn_fwd_seq.argtypes = lib.ulysses_attn_fwd.argtypes
@@ -104,7 +106,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                  "ulysses_attn_bwd",
                  "ulysses_attn_bwd_noalloc", "ulysses_attn_fwd_seq", "ulysses_attn_bwd_seq",
                  "ulysses_get_device_status", "ulysses_set_wait_limit_ns", "ulysses_selftest_wait_timeout",
-                 "ulysses_selftest_bounds"):
+                 "ulysses_selftest_bounds", "ulysses_attn_tile_order"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -330,6 +332,18 @@ def ulysses_all_to_all_head_to_seq(x_head: torch.Tensor, group=None, out: Option
 
 
 # -------------------------------------------------------------- attention
+
+def ulysses_attn_tile_order(N: int, causal: bool = True, cu_seqlens=None, for_bwd: bool = False) -> np.ndarray:
+    """The order in which the bf16 kernels walk the 128-row tiles (see
+    include/ulysses.h): every tile index once, longest walk first."""
+    n = (int(N) + 127) // 128
+    out = np.empty(max(n, 1), dtype=np.int32)
+    cu_p, nd, _keep = _cu(cu_seqlens)
+    _check("ulysses_attn_tile_order",
+           load().ulysses_attn_tile_order(int(N), int(bool(causal)), cu_p, nd, int(bool(for_bwd)),
+                                          out.ctypes.data_as(ctypes.c_void_p)))
+    return out[:n]
+
 
 def ulysses_attn_workspace_size(B: int, N: int, Hq_local: int, Hkv_local: int, d: int, num_shards: int,
                                 num_docs: int, for_bwd: bool, dtype: torch.dtype) -> int:

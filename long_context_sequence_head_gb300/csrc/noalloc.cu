@@ -63,6 +63,7 @@ uly_status ulysses_attn_bwd_noalloc(const void *q, const void *k, const void *v,
                                     int32_t causal, const int32_t *cu_seqlens_host, int32_t num_docs,
                                     float softmax_scale, uly_dtype dtype, void *stream)
 {
+    ULY_NVTX_RANGE();
     const size_t need = ulysses_attn_workspace_size(B, N, Hq_local, Hkv_local, d, num_shards,
                                                     cu_seqlens_host ? num_docs : 0, 1, dtype);
     if (need == 0)

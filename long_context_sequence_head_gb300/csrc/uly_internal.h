@@ -9,12 +9,25 @@
 #include <algorithm>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "uly_ptx.cuh"
 
 namespace uly {
 
 // cuTensorMapEncodeTiled, resolved through the runtime once per process.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+// An NVTX push/pop range around one call of the C ABI, named after the call,
+// so that profilers can attribute kernels to it.  NVTX 3 is header-only: with
+// no tool attached a push or pop is a check of a null function pointer.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define ULY_NVTX_RANGE() const ::uly::NvtxRange uly_nvtx_range_(__func__)
 
 // Device status word of the current device (2 x u32: flags, first site).
 unsigned *device_status_ptr();

@@ -104,6 +104,19 @@ WsLayout ws_layout(int64_t B, int64_t N, int Hq, int d, int S, int num_docs, boo
     return L;
 }
 
+// cu_seqlens: none (num_docs = 0), or [0 .. N] non-decreasing over num_docs >= 1 documents.
+uly_status check_docs(int64_t N, const int32_t *cu, int32_t num_docs)
+{
+    if (cu == nullptr)
+        return num_docs == 0 ? ULY_OK : ULY_ERR_INVALID_ARG;
+    if (num_docs < 1 || cu[0] != 0 || static_cast<int64_t>(cu[num_docs]) != N)
+        return ULY_ERR_INVALID_ARG;
+    for (int i = 0; i < num_docs; ++i)
+        if (cu[i + 1] < cu[i])
+            return ULY_ERR_INVALID_ARG;
+    return ULY_OK;
+}
+
 uly_status check_attn_args(int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_t d, int32_t S, int32_t causal,
                            const int32_t *cu, int32_t num_docs, uly_dtype dt)
 {
@@ -119,17 +132,7 @@ uly_status check_attn_args(int64_t B, int64_t N, int32_t Hq, int32_t Hkv, int32_
         return ULY_ERR_UNSUPPORTED;
     if (N > (int64_t(1) << 30) || static_cast<int64_t>(S) * B > (int64_t(1) << 20))
         return ULY_ERR_UNSUPPORTED;
-    if (cu == nullptr) {
-        if (num_docs != 0)
-            return ULY_ERR_INVALID_ARG;
-    } else {
-        if (num_docs < 1 || cu[0] != 0 || static_cast<int64_t>(cu[num_docs]) != N)
-            return ULY_ERR_INVALID_ARG;
-        for (int i = 0; i < num_docs; ++i)
-            if (cu[i + 1] < cu[i])
-                return ULY_ERR_INVALID_ARG;
-    }
-    return ULY_OK;
+    return check_docs(N, cu, num_docs);
 }
 
 uly_status check_swap_args(const void *a, const void *b, int64_t B, int64_t N, int32_t H, int32_t d, int32_t P,
@@ -224,6 +227,7 @@ extern "C" {
 uly_status ulysses_seq_to_head(const void *x_seq, void *x_head, int64_t B, int64_t N, int32_t H, int32_t d,
                                int32_t P, uly_dtype dtype, void *stream)
 {
+    ULY_NVTX_RANGE();
     const uly_status st = check_swap_args(x_seq, x_head, B, N, H, d, P, dtype);
     if (st != ULY_OK)
         return st;
@@ -236,6 +240,7 @@ uly_status ulysses_seq_to_head(const void *x_seq, void *x_head, int64_t B, int64
 uly_status ulysses_head_to_seq(const void *x_head, void *x_seq, int64_t B, int64_t N, int32_t H, int32_t d,
                                int32_t P, uly_dtype dtype, void *stream)
 {
+    ULY_NVTX_RANGE();
     const uly_status st = check_swap_args(x_head, x_seq, B, N, H, d, P, dtype);
     if (st != ULY_OK)
         return st;
@@ -248,6 +253,7 @@ uly_status ulysses_head_to_seq(const void *x_head, void *x_seq, int64_t B, int64
 uly_status ulysses_swap_batch(const uly_swap_desc *descs_host, int32_t n_descs, int64_t B, int64_t N, int32_t d,
                               int32_t P, uly_dtype dtype, void *stream)
 {
+    ULY_NVTX_RANGE();
     if (descs_host == nullptr || n_descs < 1 || n_descs > uly::kSwapMaxBatch)
         return ULY_ERR_INVALID_ARG;
     uly::SwapDesc descs[uly::kSwapMaxBatch];
@@ -276,6 +282,19 @@ uly_status ulysses_swap_batch(const uly_swap_desc *descs_host, int32_t n_descs, 
     if (uly::tensor_map_encoder() == nullptr || uly::device_status_ptr() == nullptr)
         return ULY_ERR_CUDA;
     return from_cuda(uly::launch_swap_batch(descs, n_descs, B, N, d, P, es, static_cast<cudaStream_t>(stream)));
+}
+
+uly_status ulysses_attn_tile_order(int64_t N, int32_t causal, const int32_t *cu_seqlens_host, int32_t num_docs,
+                                   int32_t for_bwd, int32_t *out)
+{
+    if (out == nullptr || N < 1 || N > (int64_t(1) << 30) || (causal != 0 && causal != 1) ||
+        (for_bwd != 0 && for_bwd != 1))
+        return ULY_ERR_INVALID_ARG;
+    const uly_status st = check_docs(N, cu_seqlens_host, num_docs);
+    if (st != ULY_OK)
+        return st;
+    uly::tile_order_host(for_bwd != 0, N, causal, cu_seqlens_host, num_docs, out);
+    return ULY_OK;
 }
 
 size_t ulysses_attn_workspace_size(int64_t B, int64_t N, int32_t Hq_local, int32_t Hkv_local, int32_t d,
@@ -445,6 +464,7 @@ uly_status ulysses_attn_fwd(const void *q, const void *k, const void *v, void *o
                             const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale, uly_dtype dtype,
                             void *workspace, size_t workspace_bytes, void *stream)
 {
+    ULY_NVTX_RANGE();
     return uly::attn_fwd_impl(q, k, v, o, lse, B, N, Hq_local, Hkv_local, d, num_shards, causal, cu_seqlens_host,
                          num_docs, softmax_scale, dtype, workspace, workspace_bytes, stream,
                          uly::head_rows(B, N, num_shards));
@@ -456,6 +476,7 @@ uly_status ulysses_attn_bwd(const void *q, const void *k, const void *v, const v
                             const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale, uly_dtype dtype,
                             void *workspace, size_t workspace_bytes, void *stream)
 {
+    ULY_NVTX_RANGE();
     return uly::attn_bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, N, Hq_local, Hkv_local, d, num_shards, causal,
                          cu_seqlens_host, num_docs, softmax_scale, dtype, workspace, workspace_bytes, stream,
                          uly::head_rows(B, N, num_shards));
@@ -466,6 +487,7 @@ uly_status ulysses_attn_fwd_seq(const void *q_seq, const void *k_seq, const void
                                 const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale,
                                 uly_dtype dtype, void *workspace, size_t workspace_bytes, void *stream)
 {
+    ULY_NVTX_RANGE();
     const uly_status st = check_seq_args(B, N, Hq, Hkv, d, P, dtype);
     if (st != ULY_OK)
         return st;
@@ -480,6 +502,7 @@ uly_status ulysses_attn_bwd_seq(const void *q_seq, const void *k_seq, const void
                                 const int32_t *cu_seqlens_host, int32_t num_docs, float softmax_scale,
                                 uly_dtype dtype, void *workspace, size_t workspace_bytes, void *stream)
 {
+    ULY_NVTX_RANGE();
     const uly_status st = check_seq_args(B, N, Hq, Hkv, d, P, dtype);
     if (st != ULY_OK)
         return st;
@@ -526,6 +549,7 @@ uly_status ulysses_ring_attn_fwd(const void *q_seq, const void *k_seq, const voi
                                  float softmax_scale, uly_dtype dtype, void *workspace, size_t workspace_bytes,
                                  void *stream)
 {
+    ULY_NVTX_RANGE();
     const void *ptrs[5] = {q_seq, k_seq, v_seq, o_seq, lse};
     const uly_status st = check_ring(ptrs, 5, B, N, Hq, Hkv, d, P, causal, dtype, workspace, workspace_bytes, false);
     if (st != ULY_OK)
@@ -540,6 +564,7 @@ uly_status ulysses_ring_attn_bwd(const void *q_seq, const void *k_seq, const voi
                                  float softmax_scale, uly_dtype dtype, void *workspace, size_t workspace_bytes,
                                  void *stream)
 {
+    ULY_NVTX_RANGE();
     const void *ptrs[9] = {q_seq, k_seq, v_seq, o_seq, lse, dout_seq, dq_seq, dk_seq, dv_seq};
     const uly_status st = check_ring(ptrs, 9, B, N, Hq, Hkv, d, P, causal, dtype, workspace, workspace_bytes, true);
     if (st != ULY_OK)
@@ -560,6 +585,7 @@ uly_status ulysses_sharded_ce_loss(const void *logits, const int64_t *labels, vo
                                    int32_t P, uly_dtype dtype, void *workspace, size_t workspace_bytes,
                                    void *stream)
 {
+    ULY_NVTX_RANGE();
     if (!logits || !labels || !shard_loss || !shard_good || !total_loss || !workspace)
         return ULY_ERR_INVALID_ARG;
     if (B < 1 || N < 1 || P < 1 || V < 1 || N % P != 0 || esize_of(dtype) == 0)
@@ -582,6 +608,7 @@ uly_status ulysses_sharded_ce_loss(const void *logits, const int64_t *labels, vo
 
 uly_status ulysses_get_device_status(void *stream, uint32_t *site_out)
 {
+    ULY_NVTX_RANGE();
     unsigned *p = uly::device_status_ptr();
     if (p == nullptr)
         return ULY_ERR_CUDA;
@@ -615,6 +642,7 @@ uly_status ulysses_set_wait_limit_ns(uint64_t limit_ns)
 
 uly_status ulysses_selftest_wait_timeout(uint64_t limit_ns, void *stream)
 {
+    ULY_NVTX_RANGE();
     if (limit_ns < 1000 || limit_ns > 10000000000ull)
         return ULY_ERR_INVALID_ARG;
     return from_cuda(uly::launch_selftest_timeout(limit_ns, static_cast<cudaStream_t>(stream)));
@@ -622,6 +650,7 @@ uly_status ulysses_selftest_wait_timeout(uint64_t limit_ns, void *stream)
 
 uly_status ulysses_selftest_bounds(void *stream)
 {
+    ULY_NVTX_RANGE();
 #ifdef ULY_DEBUG
     unsigned *status = uly::device_status_ptr();
     if (status == nullptr)
