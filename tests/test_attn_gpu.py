@@ -251,6 +251,39 @@ def test_running_max_speculation(uly, causal):
                       tol={"dq": max(REL_TOL["bf16"], 2.0 * floor)})
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_one_document_matches_no_documents(uly, causal):
+    """cu_seqlens = [0, N] describes the same mask as no documents, but runs
+    the kernel instances built for packed documents (tiles in the host's
+    walk order; in the forward a row's first tile from registers).  Each
+    unit computes the same thing in both, so O, lse, dK and dV must agree
+    bit for bit; dQ only up to the order of its fp32 reductions."""
+    S, N, Hq, Hkv = 2, 1000, 8, 2  # ragged tail, GQA groups of 4 (two head pairs)
+    q = _rand((S, 1, N, Hq, 128), 21, torch.bfloat16).cuda()
+    k = _rand((S, 1, N, Hkv, 128), 22, torch.bfloat16).cuda()
+    v = _rand((S, 1, N, Hkv, 128), 23, torch.bfloat16).cuda()
+    do = _rand((S, 1, N, Hq, 128), 24, torch.bfloat16).cuda()
+    out = {}
+    for name, cu in (("none", None), ("one", [0, N])):
+        g = Guards()
+        nd = 0 if cu is None else 1
+        o = g.full_like(q, float("nan"))
+        lse = g.empty((S, 1, Hq, N), torch.float32, float("nan"))
+        ws_f = g.workspace(uly.ulysses_attn_workspace_size(1, N, Hq, Hkv, 128, S, nd, False, torch.bfloat16))
+        uly.ulysses_attn_fwd(q, k, v, o, lse, causal=causal, cu_seqlens=cu, workspace=ws_f)
+        dq, dk, dv = (g.full_like(x, float("nan")) for x in (q, k, v))
+        ws_b = g.workspace(uly.ulysses_attn_workspace_size(1, N, Hq, Hkv, 128, S, nd, True, torch.bfloat16))
+        uly.ulysses_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, causal=causal, cu_seqlens=cu, workspace=ws_b)
+        torch.cuda.synchronize()
+        assert uly.ulysses_get_device_status()[0] == 0
+        g.check()
+        out[name] = (o, lse, dq, dk, dv)
+    (o0, l0, dq0, dk0, dv0), (o1, l1, dq1, dk1, dv1) = out["none"], out["one"]
+    for a, b, what in ((o0, o1, "o"), (l0, l1, "lse"), (dk0, dk1, "dk"), (dv0, dv1, "dv")):
+        assert bytes_equal(a, b), what
+    assert rel_fro(dq1, dq0) <= 1e-3, rel_fro(dq1, dq0)
+
+
 def test_one_token_documents_copy_values(uly):
     """Every document of length 1: each row attends only to itself, o_i = v_i."""
     N, Hq, Hkv = 256, 2, 1
