@@ -76,6 +76,7 @@ BF16_CASES = [
     (1, 1, 1, 2, 1, True, None),              # a single token
     (1, 1, 640, 2, 2, True, None),            # exact multiple of the tile
     (1, 1, 384, 8, 1, True, None),            # GQA group of 8: four head pairs share one KV head
+    (1, 1, 600, 4, 2, True, [0, 0, 128, 128, 300, 600, 600]),  # zero-length documents at tile edges
 ]
 
 

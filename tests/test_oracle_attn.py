@@ -61,6 +61,7 @@ CASES = [
     (1, 1, 16, 4, 1, 8, False, None),
     (2, 1, 20, 2, 1, 4, True, [0, 5, 6, 14, 20]),
     (1, 2, 11, 3, 3, 5, False, [0, 4, 11]),
+    (1, 1, 14, 2, 1, 4, True, [0, 0, 5, 5, 9, 14, 14]),  # zero-length documents: first, middle, last
 ]
 
 

@@ -65,6 +65,7 @@ def test_finite_differences(oracle_mod, causal, cu):
     (1, 1, 12, 4, 2, 8, True, None),
     (2, 2, 10, 2, 1, 4, False, None),
     (1, 1, 17, 4, 1, 4, True, [0, 7, 8, 17]),
+    (1, 1, 15, 2, 1, 4, False, [0, 0, 6, 6, 15, 15]),  # zero-length documents
 ])
 def test_matches_torch_autograd(oracle_mod, S, B, N, Hq, Hkv, d, causal, cu):
     q = _randn((S, B, N, Hq, d), 5).requires_grad_()

@@ -60,12 +60,14 @@ def test_without_documents_is_index_order(uly, causal, for_bwd):
 
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("for_bwd", [False, True])
-@pytest.mark.parametrize("case", ["one-token docs", "straddling", "recipe"])
+@pytest.mark.parametrize("case", ["one-token docs", "straddling", "zero-length docs", "recipe"])
 def test_documents_longest_walk_first(uly, causal, for_bwd, case):
     if case == "one-token docs":
         N, cu = 700, [0, 100, 101, 350, 700]
     elif case == "straddling":
         N, cu = 1500, [0, 129, 300, 301, 1100, 1500]
+    elif case == "zero-length docs":
+        N, cu = 900, [0, 0, 128, 128, 300, 900, 900]
     else:
         N = 4096
         cu = list(cu_seqlens_from_lengths(doc_lengths(N, 4, seed=5, lo=64, hi=900)))
