@@ -77,6 +77,8 @@ BF16_CASES = [
     (1, 1, 640, 2, 2, True, None),            # exact multiple of the tile
     (1, 1, 384, 8, 1, True, None),            # GQA group of 8: four head pairs share one KV head
     (1, 1, 600, 4, 2, True, [0, 0, 128, 128, 300, 600, 600]),  # zero-length documents at tile edges
+    (2, 2, 384, 4, 2, True, [0, 200, 384]),   # documents with two shards and two batches
+    (1, 1, 300, 3, 1, False, [0, 150, 300]),  # documents with an odd group (one head has no partner)
 ]
 
 
