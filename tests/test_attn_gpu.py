@@ -348,3 +348,35 @@ def test_wait_timeout_reports_status(uly):
     assert uly.ulysses_get_device_status()[0] == 0  # cleared
     x = torch.arange(16, dtype=torch.float32, device="cuda")
     assert float(x.sum()) == 120.0
+
+
+def _random_cases(n, seed=1234):
+    """Seeded random shapes: shards, batches, ragged lengths, GQA groups of
+    1-8, causal or not, and documents (none, or lengths >= 8 with a
+    zero-length document sometimes in between)."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        S, B = int(rng.integers(1, 3)), int(rng.integers(1, 3))
+        N = int(rng.integers(2, 700))
+        Hkv = int(rng.integers(1, 3))
+        G = int(rng.choice([1, 2, 3, 4, 8]))
+        causal = bool(rng.integers(0, 2))
+        cu = None
+        if i % 2 == 1 and N >= 16:  # every other case packs documents
+            cu, t = [0], 0
+            while t < N:
+                L = min(int(rng.integers(8, max(9, N // 2))), N - t)
+                t += L
+                cu.append(t)
+                if rng.integers(0, 4) == 0:
+                    cu.append(t)  # a zero-length document
+            if N - (cu[-1] - cu[-2]) > 0 and cu[-1] - cu[-2] < 8 and len(cu) > 2:
+                cu.pop(-2)  # keep the last real document at least 8 long
+        cases.append((S, B, N, G * Hkv, Hkv, causal, cu))
+    return cases
+
+
+@pytest.mark.parametrize("S,B,N,Hq,Hkv,causal,cu", _random_cases(12))
+def test_random_shapes_vs_oracle(uly, S, B, N, Hq, Hkv, causal, cu):
+    _attn_case(uly, S, B, N, Hq, Hkv, 128, torch.bfloat16, causal, cu, seed=5)
