@@ -88,3 +88,23 @@ def test_swap_batch_bit_exact(uly, oracle_mod, dtype, P, B, N, Hq, Hkv, d):
     st, site = uly.ulysses_get_device_status()
     assert st == 0, hex(site)
     G.check()
+
+
+def _random_swap_cases(n, seed=99):
+    """Seeded random swap shapes: P in 1..8, H a multiple of P (up to 64
+    heads), N a multiple of P (ragged token chunks), B in 1..3, d 64 or 128."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        P = int(rng.choice([1, 2, 3, 4, 8]))
+        H = P * int(rng.integers(1, max(2, 64 // P + 1)))
+        N = P * int(rng.integers(1, 400))
+        out.append((P, int(rng.integers(1, 4)), N, H, int(rng.choice([64, 128]))))
+    return out
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("P,B,N,H,d", _random_swap_cases(8))
+def test_swap_random_shapes_bit_exact(uly, oracle_mod, dtype, P, B, N, H, d):
+    test_swap_bit_exact(uly, oracle_mod, dtype, P, B, N, H, d)
