@@ -100,3 +100,25 @@ def test_fused_bench_workload_sampled(uly, oracle_mod):
     log_errors("fused seq qwen3_4b_n65536 sampled", **errs)
     assert errs["o"] <= REL_TOL["bf16"] and errs["dq"] <= REL_TOL["bf16"], errs
     assert errs["lse_max_abs"] <= LSE_TOL["bf16"], errs
+
+
+def _random_fused_cases(n, seed=77):
+    """Seeded random fused-layout shapes with the Qwen3-4B head counts: P in
+    {1, 2, 4, 8}, N/P a multiple of 128 (the bf16 path's requirement), and
+    documents whose boundaries fall anywhere (across shard boundaries too)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        P = int(rng.choice([1, 2, 4, 8]))
+        N = P * 128 * int(rng.integers(1, max(2, 1536 // (P * 128) + 1)))
+        cu = None
+        if i % 2 == 0:
+            cuts = sorted(set(int(c) for c in rng.integers(1, N, size=int(rng.integers(1, 5)))))
+            cu = [0] + cuts + [N]
+        out.append((N, P, cu))
+    return out
+
+
+@pytest.mark.parametrize("N,P,cu", _random_fused_cases(4))
+def test_fused_random_shapes_vs_oracle(uly, oracle_mod, N, P, cu):
+    test_fused_vs_oracle(uly, oracle_mod, "qwen3_4b_n8192", N, P, cu)
