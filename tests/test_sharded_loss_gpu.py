@@ -90,3 +90,25 @@ def test_all_ignored_and_invalid_labels(uly):
     labels[0, 0, 3] = V + 5  # out of range: ignored and reported
     uly.ulysses_sharded_ce_loss(logits.cuda(), labels.cuda(), P)
     assert uly.ulysses_get_device_status()[0] == 1   # ULY_ERR_INVALID_ARG
+
+
+def _random_loss_cases(n, seed=31):
+    """Seeded random loss shapes: P in 1..8, batches, vocabularies from a few
+    entries to beyond Qwen3's (multiples of 8 or not: vector and scalar paths,
+    every cluster size), both dtypes."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        P = int(rng.choice([1, 2, 4, 8]))
+        N = P * int(rng.integers(1, 64 // P + 2))
+        V = int(rng.choice([int(rng.integers(2, 600)), int(rng.integers(1000, 200000))]))
+        if rng.integers(0, 2) and V >= 8:
+            V -= V % 8  # a multiple of 8: the 16-byte vector path (clusters with the gradient)
+        dtype = torch.bfloat16 if rng.integers(0, 2) else torch.float32
+        out.append((P, int(rng.integers(1, 3)), N, V, dtype))
+    return out
+
+
+@pytest.mark.parametrize("P,B,N,V,dtype", _random_loss_cases(6))
+def test_sharded_ce_random_shapes(uly, P, B, N, V, dtype):
+    test_sharded_ce_vs_oracle(uly, P, B, N, V, dtype)
