@@ -105,3 +105,21 @@ def test_ring_bench_workload_sampled(uly, oracle_mod):
     log_errors("ring qwen3_4b_n65536 sampled", **errs)
     assert errs["o"] <= REL_TOL["bf16"] and errs["dq"] <= REL_TOL["bf16"], errs
     assert errs["lse_max_abs"] <= LSE_TOL["bf16"], errs
+
+
+def _random_ring_cases(n, seed=55):
+    """Seeded random ring shapes with the Qwen3-4B head counts: P a divisor
+    of the 8 KV heads (1, 2, 4, 8), N a multiple of P with ragged chunks,
+    causal or not."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        P = int(rng.choice([1, 2, 4, 8]))
+        out.append(("qwen3_4b_n8192", P * int(rng.integers(20, 160)), P, bool(rng.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("name,N,P,causal", _random_ring_cases(4))
+def test_ring_random_shapes_vs_oracle(uly, name, N, P, causal):
+    test_ring_vs_oracle(uly, name, N, P, causal)
